@@ -1,0 +1,543 @@
+"""Benchmark of the fused CFG sampler step on one B300 (or N replicas under torchrun).
+
+A "step" is one call of the fused step kernel: rel-MAE + schedule update +
+guidance + DDIM/Euler update over the whole latent of one batch.  The
+default workload is SDXL 1024px, batch 8 (latent 8x4x128x128, bf16 storage,
+50-step DDIM, w = 5).  Inputs are synthetic and resident in HBM; the timed
+steps rotate over enough buffer sets that every step's inputs come from HBM
+(not the 126 MB L2), and are replayed from CUDA graphs.
+
+Prints ONE JSON line (rank 0):
+  value / unit       latent elements per second per step, whole job
+  roofline           algorithmic HBM bytes / measured step time vs the measured copy peak
+  e2e                the same metric through the public Python API with pinned host
+                     buffers, host->device and device->host copies inside the timed region
+  cpu_baseline       the CPU oracle timed on a bounded sample (rank 0, N = 1)
+  sweep              the same device measurement on every other workload (rank 0, N = 1)
+
+``--impl reference`` times the CPU oracle instead (the slow reference program)
+and prints the same kind of line with ``"impl": "reference"``.
+
+Multi-GPU: the step needs no exchange on one latent per GPU, so N ranks run N
+independent replicas (weak scaling): barrier, time, max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import workloads as W  # noqa: E402
+
+DEFAULT_WORKLOAD = "sdxl_1024_b8_bf16"
+FALLBACK_HBM_GBS = 6400.0
+PROFILE_DIR = ROOT / "profiles"
+KERNEL_SRC = ROOT / "cfg_guided_sampler_step_b300" / "csrc" / "cfgstep.cu"
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (replicas only; no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# Peaks, profiles, clocks
+# ---------------------------------------------------------------------------
+def hbm_peak():
+    p = ROOT / "MEASURED_PEAKS.json"
+    try:
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:  # noqa: BLE001 - absent or unreadable: the documented fallback
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    return hashlib.sha256(KERNEL_SRC.read_bytes()).hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
+    f = PROFILE_DIR / f"cfg_step_kernel_{workload}.md"
+    if not f.exists():
+        return None
+    text = f.read_text()
+    m_src = re.search(r"kernel source sha256\[:16\]\s*\|\s*`?([0-9a-f]{16})", text)
+    m_b = re.search(r"dram bytes per launch \(read \+ write\)\s*\|\s*([0-9][0-9,]*)", text)
+    if not m_src or not m_b or m_src.group(1) != kernel_source_hash():
+        return None
+    return int(m_b.group(1).replace(",", ""))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("timestamp,index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark_begin(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 11:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + f[0].split(".")[1]) if "." in f[0] else 0.0
+            except (ValueError, IndexError):
+                continue
+            if self.t0 is not None and not (self.t0 - 0.05 <= ts <= self.t1 + 0.05):
+                continue
+            n += 1
+            try:
+                sm.append(float(f[3]))
+                smax.append(float(f[4]))
+            except ValueError:
+                pass
+            for name, val in zip(names, f[7:11]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ---------------------------------------------------------------------------
+# The device measurement
+# ---------------------------------------------------------------------------
+def step_plan(wl: W.Workload, cs):
+    """Per-step (step index, coefficients) of one sampler run of the workload."""
+    N = wl.n_steps
+    if wl.mode == "ddim":
+        abar = cs.abar_linear(wl.T, wl.beta_start, wl.beta_end)
+        ts = cs.ddim_timesteps(N, wl.T)
+        return [dict(step=s, abar_t=float(abar[ts[s]]),
+                     abar_prev=float(abar[ts[s + 1]]) if s + 1 < N else 1.0) for s in range(N)]
+    return [dict(step=s, t_cur=1.0 - s / N, t_next=1.0 - (s + 1) / N) for s in range(N)]
+
+
+def enqueue_step(cs, wl, bufs, plan_s, ws, st, sp, M=None):
+    x, pc, pu = bufs[:3]
+    xo = bufs[3] if len(bufs) > 3 else x
+    if wl.mode == "ddim":
+        cs.ddim_step(xo, x, pc, pu, w=wl.w, abar_t=plan_s["abar_t"], abar_prev=plan_s["abar_prev"],
+                     eta=wl.eta, seed=wl.seed, step=plan_s["step"], M_out=M, state=st, sched=sp,
+                     workspace=ws)
+    else:
+        cs.flow_step(xo, x, pc, pu, w=wl.w, t_cur=plan_s["t_cur"], t_next=plan_s["t_next"],
+                     step=plan_s["step"], M_out=M, state=st, sched=sp, workspace=ws)
+
+
+def make_sets(wl, n_sets, device, torch):
+    dt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
+    g = torch.Generator(device=device)
+    g.manual_seed(wl.seed)
+    sets = []
+    for _ in range(n_sets):
+        x = torch.randn(wl.n, generator=g, device=device, dtype=torch.float32).to(dt)
+        pu = torch.randn(wl.n, generator=g, device=device, dtype=torch.float32).to(dt)
+        pc = (pu.float() + 0.1 * torch.randn(wl.n, generator=g, device=device)).to(dt)
+        sets.append((x, pc, pu, torch.empty_like(x)))
+    return sets
+
+
+def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clocks=None):
+    """Time exactly `steps` fused steps (plus `warmup` untimed) over rotating HBM-resident sets."""
+    import torch
+    import cfg_guided_sampler_step_b300 as cs
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2**20))
+    set_bytes = 4 * wl.n * wl.elem_bytes          # x_in, pred_c, pred_u, x_out
+    n_sets = max(2, math.ceil(4 * l2 / set_bytes))
+    sets = make_sets(wl, n_sets, device, torch)
+    code = cs.CFG_F32 if wl.dtype == "f32" else cs.CFG_BF16
+    ws = cs.new_workspace(wl.n, code, device)
+    st = cs.new_sched_state(device)
+    sp = cs.SchedParams(n_steps=wl.n_steps, L=wl.L, g_slope=wl.g_slope, k=wl.k, tau_cap=wl.tau_cap)
+    plan = step_plan(wl, cs)
+    # graph step j uses buffer set j % n_sets (read x_in, pred_c, pred_u; write x_out) and
+    # sampler step j % N.  A graph is a whole number of rotations, so a set is reused only
+    # after every other set has passed (>= 4x L2 of traffic in between).
+    G = n_sets * max(1, round(4 * max(n_sets, wl.n_steps) / n_sets))
+
+    def capture(count):
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device)
+        s.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(s):
+            for j in range(min(count, 8)):          # eager warm-up of the launch path
+                enqueue_step(cs, wl, sets[j % n_sets], plan[j % wl.n_steps], ws, st, sp)
+        torch.cuda.current_stream(device).wait_stream(s)
+        torch.cuda.synchronize(device)
+        with torch.cuda.graph(g, stream=s):
+            for j in range(count):
+                enqueue_step(cs, wl, sets[j % n_sets], plan[j % wl.n_steps], ws, st, sp)
+        torch.cuda.synchronize(device)
+        return g
+
+    if steps < G:
+        G = steps
+    g_full = capture(G) if G > 0 else None
+    rem = steps % G if G else 0
+    g_rem = capture(rem) if rem else None
+    full_reps = steps // G if G else 0
+    w_full, w_rem = divmod(max(warmup, 0), G) if G else (0, 0)
+    g_wrem = capture(w_rem) if w_rem else None
+    stream = torch.cuda.current_stream(device)
+    for _ in range(w_full):
+        g_full.replay()
+    if g_wrem is not None:
+        g_wrem.replay()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if clocks:
+        clocks.mark_begin()
+    start.record(stream)
+    for _ in range(full_reps):
+        g_full.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    end.record(stream)
+    end.synchronize()
+    torch.cuda.synchronize(device)
+    if clocks:
+        clocks.mark_end()
+    barrier(world)
+    ms = start.elapsed_time(end)
+    state = cs.read_sched_state(st)
+    return {"ms": ms, "n_sets": n_sets, "set_bytes": set_bytes, "l2_bytes": l2,
+            "graph_steps": G, "launches": steps, "state_flags": state["flags"]}
+
+
+def time_e2e(wl: W.Workload, steps: int, device):
+    """Same metric through the public API with pinned host inputs and a host read of each result."""
+    import torch
+    import cfg_guided_sampler_step_b300 as cs
+    dt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
+    inp = W.draw_prediction_pair(wl.n, wl.dtype, wl.seed)
+
+    def host(a):
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+        t = t.view(dt) if a.dtype == np.uint16 else t
+        return t.pin_memory()
+
+    hx, hc, hu = host(inp["x"]), host(inp["c"]), host(inp["u"])
+    hout = torch.empty(wl.n, dtype=dt).pin_memory()
+    hM = torch.empty(1, dtype=torch.float64).pin_memory()
+    dx = torch.empty(wl.n, dtype=dt, device=device)
+    dc, du = torch.empty_like(dx), torch.empty_like(dx)
+    dM = torch.zeros(1, dtype=torch.float64, device=device)
+    ws = cs.new_workspace(wl.n, cs.CFG_F32 if wl.dtype == "f32" else cs.CFG_BF16, device)
+    st = cs.new_sched_state(device)
+    sp = cs.SchedParams(n_steps=wl.n_steps, L=wl.L, g_slope=wl.g_slope, k=wl.k, tau_cap=wl.tau_cap)
+    plan = step_plan(wl, cs)
+
+    def one(i):
+        dx.copy_(hx, non_blocking=True)
+        dc.copy_(hc, non_blocking=True)
+        du.copy_(hu, non_blocking=True)
+        enqueue_step(cs, wl, (dx, dc, du), plan[i % wl.n_steps], ws, st, sp, M=dM)
+        hout.copy_(dx, non_blocking=True)
+        hM.copy_(dM, non_blocking=True)
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize(device)
+    stream = torch.cuda.current_stream(device)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        one(i)
+    end.record(stream)
+    end.synchronize()
+    ms = start.elapsed_time(end)
+    eb = wl.elem_bytes
+    return {"value": wl.n * steps / (ms * 1e-3), "unit": "latent elements/s",
+            "h2d_bytes_per_step": 3 * wl.n * eb, "d2h_bytes_per_step": wl.n * eb + 8,
+            "steps": steps, "ms_per_step": ms / steps}
+
+
+# ---------------------------------------------------------------------------
+# The oracle (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_step_fn(wl: W.Workload, n_sample: int):
+    """One oracle step of the workload on the first n_sample elements (stored inputs)."""
+    from oracle import cfg_oracle as O
+    inp = W.draw_prediction_pair(n_sample, wl.dtype, wl.seed)
+    x = W.stored_to_f64(inp["x"], wl.dtype)
+    c = W.stored_to_f64(inp["c"], wl.dtype)
+    u = W.stored_to_f64(inp["u"], wl.dtype)
+    if wl.mode == "ddim":
+        abar = O.abar_linear(wl.T, wl.beta_start, wl.beta_end)
+        ts = O.ddim_timesteps(wl.n_steps, wl.T)
+        sched = [(float(abar[ts[s]]), float(abar[ts[s + 1]]) if s + 1 < wl.n_steps else 1.0)
+                 for s in range(wl.n_steps)]
+
+        def fn(i):
+            s = i % wl.n_steps
+            ab, abp = sched[s]
+            return O.ddim_step(x, c, u, wl.dtype, wl.w, ab, abp, wl.eta, wl.seed, s,
+                               last=(s == wl.n_steps - 1))
+    else:
+        t = O.flow_times(wl.n_steps)
+
+        def fn(i):
+            s = i % wl.n_steps
+            return O.flow_step(x, c, u, wl.dtype, wl.w, float(t[s]), float(t[s + 1]))
+    return fn
+
+
+def time_oracle(wl: W.Workload, steps: int, warmup: int, budget_s: float):
+    """Time `steps` oracle steps, each on a sample sized so the run fits in about budget_s."""
+    probe_n = min(wl.n, 1 << 16)
+    fn = oracle_step_fn(wl, probe_n)
+    t0 = time.perf_counter()
+    fn(0)
+    t_probe = time.perf_counter() - t0
+    fn_small = oracle_step_fn(wl, 64)
+    t0 = time.perf_counter()
+    for i in range(5):
+        fn_small(i)
+    t_fixed = (time.perf_counter() - t0) / 5
+    per_elem = max((t_probe - t_fixed) / probe_n, 1e-10)
+    per_step_budget = budget_s / max(steps + warmup, 1)
+    n_sample = int((per_step_budget - t_fixed) / per_elem)
+    n_sample = max(64, min(wl.n, n_sample))
+    fn = oracle_step_fn(wl, n_sample)
+    for i in range(warmup):
+        fn(i)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        fn(i)
+    dt = time.perf_counter() - t0
+    return {"value": n_sample * steps / dt, "n_sample": n_sample, "seconds": dt, "steps": steps}
+
+
+def oracle_threads() -> int:
+    # numpy elementwise ufuncs and np.sum run on one thread; no BLAS call is on this path
+    return 1
+
+
+# ---------------------------------------------------------------------------
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400_000)
+    ap.add_argument("--warmup", type=int, default=4_000)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.WORKLOAD_ORDER)
+    ap.add_argument("--impl", default="cfgstep", choices=["cfgstep", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--sweep-steps", type=int, default=60_000)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    world, rank, local = dist_env()
+    wl = W.WORKLOADS[args.workload]
+    warmup = max(args.warmup, 3)
+    metric = "latent elements/s per CFG sampler step"
+    unit = "latent elements/s"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        budget = min(150.0, 20.0 + 1e-4 * (args.steps + warmup))
+        r = time_oracle(wl, args.steps, warmup, budget)
+        sample = (f"oracle step (fp64 NumPy: rel-MAE, guidance, {wl.mode} update, {wl.dtype} "
+                  f"rounding) on {r['n_sample']} of the {wl.n} latent elements per step")
+        line = {"impl": "reference", "metric": metric, "value": r["value"], "unit": unit,
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": warmup,
+                "ms_per_step": 1e3 * r["seconds"] / max(args.steps, 1), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": workload_config(wl),
+                "cpu_baseline": {"value": r["value"], "unit": unit, "cores": oracle_threads(),
+                                 "kind": "oracle", "sample": sample},
+                "e2e": {"value": r["value"], "unit": unit, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}), flush=True)
+        return 1
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    import cfg_guided_sampler_step_b300 as cs  # noqa: F401  (fails loudly if not built)
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:  # noqa: BLE001
+        uuid = None
+    clocks = ClockSampler(uuid) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    dev = time_device(wl, args.steps, warmup, device, world, clocks)
+    clk = clocks.stop() if clocks else None
+    ms = max_over_ranks(dev["ms"], world, device)
+    total_elems = sum_over_ranks(float(wl.n * args.steps), world, device)
+    value = total_elems / (ms * 1e-3)
+    per_launch_s = dev["ms"] * 1e-3 / max(args.steps, 1)
+    peak, peak_kind = hbm_peak()
+    achieved = wl.bytes_per_step / per_launch_s / 1e9
+    e2e = time_e2e(wl, args.e2e_steps, device)
+    e2e_v = sum_over_ranks(e2e["value"], world, device)
+    if rank != 0:
+        return 0
+    line = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(workload_config(wl), parallelism=f"replicas{world}",
+                       l2=f"rotating {dev['n_sets']} buffer sets of {dev['set_bytes']} B "
+                          f"({dev['n_sets'] * dev['set_bytes'] / 2**20:.0f} MiB >= 4x the "
+                          f"{dev['l2_bytes'] / 2**20:.0f} MiB L2)",
+                       launch=f"CUDA graphs of {dev['graph_steps']} steps, programmatic dependent launch"),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(wl.name),
+                     "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.4 TB/s",
+                     "algorithmic_bytes_per_launch": wl.bytes_per_step,
+                     "frac_of_8tbs_spec": achieved / 8000.0},
+        "e2e": {"value": e2e_v, "unit": e2e["unit"], "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if world == 1 and not args.no_sweep:
+        sweep = {}
+        for name in W.WORKLOAD_ORDER:
+            if name == wl.name:
+                continue
+            w2 = W.WORKLOADS[name]
+            d2 = time_device(w2, args.sweep_steps, 2000, device, 1)
+            s = d2["ms"] * 1e-3 / args.sweep_steps
+            sweep[name] = {"value": w2.n / s, "us_per_step": s * 1e6,
+                           "achieved_gbs": w2.bytes_per_step / s / 1e9,
+                           "frac": w2.bytes_per_step / s / 1e9 / peak,
+                           "traffic": profiled_traffic(name)}
+        line["sweep"] = sweep
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(wl: W.Workload, seconds: float):
+    """The oracle's step on the full latent, repeated for about `seconds` on one host core."""
+    fn = oracle_step_fn(wl, wl.n)
+    fn(0)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        fn(reps)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": wl.n * reps / dt, "unit": "latent elements/s", "cores": oracle_threads(),
+            "kind": "oracle",
+            "sample": f"{reps} oracle steps (fp64 NumPy) on the full {wl.n}-element latent, {dt:.1f} s"}
+
+
+def workload_config(wl: W.Workload):
+    return {"workload": wl.name, "shape": list(wl.shape), "n": wl.n, "storage": wl.dtype,
+            "sampler": (f"DDIM eta={wl.eta} {wl.n_steps} steps" if wl.mode == "ddim"
+                        else f"Euler flow {wl.n_steps} steps"),
+            "w": wl.w, "global_batch": wl.shape[0]}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

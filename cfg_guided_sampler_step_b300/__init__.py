@@ -1,0 +1,315 @@
+"""Python binding of the CFG sampler-step library (``libcfgstep.so``).
+
+Argument marshalling only: every entry point forwards device pointers, sizes
+and the current CUDA stream to the C ABI declared in ``include/cfgstep.h``;
+all arithmetic of the step runs in the library's CUDA kernels.  PyTorch is
+used for device memory and streams.
+
+The library must be built (``python -m cfg_guided_sampler_step_b300._build``
+or ``__graft_entry__.build()``); importing this package raises if it is
+missing -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from ctypes import (CFUNCTYPE, POINTER, Structure, c_char_p, c_double, c_float, c_int32, c_int64,
+                    c_size_t, c_uint8, c_uint32, c_uint64, c_void_p)
+from pathlib import Path
+from typing import Callable, Dict, Optional
+
+import numpy as np
+
+__all__ = [
+    "CFG_F32", "CFG_BF16", "CFG_MODE_DDIM", "CFG_MODE_FLOW", "TAU_NONE", "SCHED_MAX_STEPS",
+    "CfgError", "SchedParams", "lib", "lib_path", "workspace_bytes", "new_workspace",
+    "new_sched_state", "read_sched_state", "relmae_reduce", "ddim_step", "flow_step",
+    "sched_observe", "randn", "abar_linear", "ddim_timesteps", "sampler_run", "version",
+]
+
+CFG_F32, CFG_BF16 = 0, 1
+CFG_MODE_DDIM, CFG_MODE_FLOW = 0, 1
+TAU_NONE = 2**31 - 1
+SCHED_MAX_STEPS = 1024
+STATUS_NAMES = {0: "CFG_OK", -1: "CFG_ERR_INVALID_ARG", -2: "CFG_ERR_UNSUPPORTED_DTYPE",
+                -3: "CFG_ERR_WORKSPACE", -4: "CFG_ERR_CUDA", -5: "CFG_ERR_CALLBACK"}
+
+lib_path = Path(__file__).resolve().parent / "libcfgstep.so"
+
+
+class CfgError(RuntimeError):
+    """A negative status from the library, with its message."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class SchedParamsC(Structure):
+    _fields_ = [("L", c_int32), ("k", c_int32), ("g_slope", c_double), ("tau_cap", c_int32),
+                ("n_steps", c_int32)]
+
+
+class SchedStateC(Structure):
+    _fields_ = [("n_seen", c_int32), ("tau1p", c_int32), ("argmin", c_int32), ("tau_cap", c_int32),
+                ("tau1", c_int32), ("tau2", c_int32), ("decided_at", c_int32), ("flags", c_uint32),
+                ("min_M", c_double), ("M", c_double * SCHED_MAX_STEPS),
+                ("G", c_double * SCHED_MAX_STEPS), ("phase", c_uint8 * SCHED_MAX_STEPS)]
+
+
+DENOISE_FN = CFUNCTYPE(c_int32, c_void_p, c_int32, c_int32, c_double, c_void_p, c_void_p, c_void_p,
+                       c_void_p)
+
+
+def _load() -> ctypes.CDLL:
+    if not lib_path.exists():
+        raise ImportError(
+            f"{lib_path} is not built; run `python -m cfg_guided_sampler_step_b300._build` "
+            "(needs nvcc). There is no CPU fallback.")
+    L = ctypes.CDLL(str(lib_path))
+    vp = c_void_p
+    sigs = {
+        "cfg_last_error": (c_char_p, []),
+        "cfg_version": (c_char_p, []),
+        "cfg_workspace_bytes": (c_size_t, [c_int64, c_int32]),
+        "cfg_workspace_init": (c_int32, [vp, c_size_t, vp]),
+        "cfg_relmae_reduce": (c_int32, [vp, vp, c_int64, c_int32, vp, vp, POINTER(SchedParamsC),
+                                        c_int32, vp, c_size_t, vp]),
+        "cfg_ddim_step": (c_int32, [vp, vp, vp, vp, c_int64, c_int32, c_float, c_double, c_double,
+                                    c_float, c_uint64, c_int32, vp, vp, POINTER(SchedParamsC), vp,
+                                    c_size_t, vp]),
+        "cfg_flow_step": (c_int32, [vp, vp, vp, vp, c_int64, c_int32, c_float, c_double, c_double,
+                                    c_int32, vp, vp, POINTER(SchedParamsC), vp, c_size_t, vp]),
+        "cfg_sched_observe": (c_int32, [vp, POINTER(SchedParamsC), c_int32, c_double, vp]),
+        "cfg_randn": (c_int32, [vp, c_int64, c_uint64, c_uint32, c_uint32, vp]),
+        "cfg_abar_linear": (c_int32, [POINTER(c_double), c_int32, c_double, c_double]),
+        "cfg_ddim_timesteps": (c_int32, [POINTER(c_int32), c_int32, c_int32]),
+        "cfg_sampler_run": (c_int32, [vp, c_int64, c_int32, c_int32, POINTER(c_double), c_int32,
+                                      POINTER(c_int32), POINTER(c_double), c_int32, c_float,
+                                      c_float, c_uint64, DENOISE_FN, vp, vp, vp,
+                                      POINTER(SchedParamsC), vp, c_int32, vp, c_size_t, vp]),
+    }
+    for name, (res, args) in sigs.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
+lib = _load()
+
+
+def version() -> str:
+    return lib.cfg_version().decode()
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise CfgError(status, lib.cfg_last_error().decode())
+
+
+# ---------------------------------------------------------------------------
+# torch plumbing
+# ---------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return CFG_F32
+    if t.dtype == torch.bfloat16:
+        return CFG_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _dev_ptr(t, name: str) -> int:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class SchedParams:
+    """tau1/tau2 rule parameters (L, k, g_slope, tau_cap, n_steps); see cfg_sched_params."""
+
+    def __init__(self, n_steps: int, L: int = 5, g_slope: float = 1e-3, k: int = 10,
+                 tau_cap: int = -1):
+        self.c = SchedParamsC(L=L, k=k, g_slope=g_slope, tau_cap=tau_cap, n_steps=n_steps)
+
+    def __repr__(self) -> str:
+        c = self.c
+        return f"SchedParams(n_steps={c.n_steps}, L={c.L}, g_slope={c.g_slope}, k={c.k}, tau_cap={c.tau_cap})"
+
+
+def _sp(sched: Optional[SchedParams]):
+    return None if sched is None else ctypes.byref(sched.c)
+
+
+def workspace_bytes(n: int, dtype_code: int) -> int:
+    return int(lib.cfg_workspace_bytes(n, dtype_code))
+
+
+def new_workspace(n: int = 0, dtype_code: int = CFG_BF16, device=None):
+    """A zero-filled (hence prepared) device workspace for calls over n elements."""
+    torch = _torch()
+    nb = workspace_bytes(n, dtype_code)
+    if nb == 0:
+        raise ValueError("invalid n / dtype for a workspace")
+    return torch.zeros(nb, dtype=torch.uint8, device=device or "cuda")
+
+
+def new_sched_state(device=None):
+    """Device memory for one cfg_sched_state (contents are reset by step 0)."""
+    torch = _torch()
+    return torch.zeros(ctypes.sizeof(SchedStateC), dtype=torch.uint8, device=device or "cuda")
+
+
+def read_sched_state(state) -> Dict[str, object]:
+    """Copy a device schedule state to the host (synchronises the current stream)."""
+    host = state.detach().to("cpu").numpy().tobytes()
+    s = SchedStateC.from_buffer_copy(host)
+    n = max(0, min(s.n_seen, SCHED_MAX_STEPS))
+    return {
+        "n_seen": s.n_seen, "tau1p": s.tau1p, "argmin": s.argmin, "tau_cap": s.tau_cap,
+        "tau1": s.tau1, "tau2": s.tau2, "decided_at": s.decided_at, "flags": s.flags,
+        "min_M": s.min_M,
+        "M": np.array(s.M[:n], dtype=np.float64),
+        "G": np.array(s.G[:n], dtype=np.float64),
+        "phase": np.array(s.phase[:n], dtype=np.uint8),
+    }
+
+
+def _ws(workspace):
+    return _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size()
+
+
+# ---------------------------------------------------------------------------
+# Entry points
+# ---------------------------------------------------------------------------
+def relmae_reduce(pred_c, pred_u, *, workspace, M_out=None, state=None, sched=None, step: int = 0,
+                  stream=None) -> None:
+    """rel-MAE of (pred_c, pred_u) into M_out (float64 device scalar) and/or the schedule."""
+    if pred_c.shape != pred_u.shape or pred_c.dtype != pred_u.dtype:
+        raise ValueError("pred_c and pred_u must match in shape and dtype")
+    ws, wsb = _ws(workspace)
+    _check(lib.cfg_relmae_reduce(_dev_ptr(pred_c, "pred_c"), _dev_ptr(pred_u, "pred_u"),
+                                 pred_c.numel(), _dtype_code(pred_c), _dev_ptr(M_out, "M_out"),
+                                 _dev_ptr(state, "state"), _sp(sched), step, ws, wsb,
+                                 _stream(stream)))
+
+
+def _same(x_out, x_in, pc, pu) -> None:
+    for t in (x_in, pc, pu):
+        if t.shape != x_out.shape or t.dtype != x_out.dtype:
+            raise ValueError("x_out, x_in, pred_c, pred_u must share shape and dtype")
+
+
+def ddim_step(x_out, x_in, pred_c, pred_u, *, w: float, abar_t: float, abar_prev: float,
+              workspace, eta: float = 0.0, seed: int = 0, step: int = 0, M_out=None, state=None,
+              sched=None, stream=None) -> None:
+    """One fused CFG + DDIM step (see cfg_ddim_step)."""
+    _same(x_out, x_in, pred_c, pred_u)
+    ws, wsb = _ws(workspace)
+    _check(lib.cfg_ddim_step(_dev_ptr(x_out, "x_out"), _dev_ptr(x_in, "x_in"),
+                             _dev_ptr(pred_c, "pred_c"), _dev_ptr(pred_u, "pred_u"), x_out.numel(),
+                             _dtype_code(x_out), w, abar_t, abar_prev, eta, seed, step,
+                             _dev_ptr(M_out, "M_out"), _dev_ptr(state, "state"), _sp(sched), ws,
+                             wsb, _stream(stream)))
+
+
+def flow_step(x_out, x_in, v_c, v_u, *, w: float, t_cur: float, t_next: float, workspace,
+              step: int = 0, M_out=None, state=None, sched=None, stream=None) -> None:
+    """One fused CFG + Euler flow step (see cfg_flow_step)."""
+    _same(x_out, x_in, v_c, v_u)
+    ws, wsb = _ws(workspace)
+    _check(lib.cfg_flow_step(_dev_ptr(x_out, "x_out"), _dev_ptr(x_in, "x_in"), _dev_ptr(v_c, "v_c"),
+                             _dev_ptr(v_u, "v_u"), x_out.numel(), _dtype_code(x_out), w, t_cur,
+                             t_next, step, _dev_ptr(M_out, "M_out"), _dev_ptr(state, "state"),
+                             _sp(sched), ws, wsb, _stream(stream)))
+
+
+def sched_observe(state, sched: SchedParams, step: int, M: float, stream=None) -> None:
+    """Record an externally computed rel-MAE value as step ``step`` of the schedule."""
+    _check(lib.cfg_sched_observe(_dev_ptr(state, "state"), _sp(sched), step, M, _stream(stream)))
+
+
+def randn(out, *, seed: int, step: int = 0, stream_id: int = 0, stream=None) -> None:
+    """Fill a float32 device tensor with the library's Philox/Box-Muller N(0,1) stream."""
+    torch = _torch()
+    if out.dtype != torch.float32:
+        raise TypeError("randn writes float32")
+    _check(lib.cfg_randn(_dev_ptr(out, "out"), out.numel(), seed, step, stream_id, _stream(stream)))
+
+
+def abar_linear(T: int = 1000, beta_start: float = 1e-4, beta_end: float = 0.02) -> np.ndarray:
+    """Host table abar[t] of the linear-beta schedule (computed by the library)."""
+    out = np.empty(T, dtype=np.float64)
+    _check(lib.cfg_abar_linear(out.ctypes.data_as(POINTER(c_double)), T, beta_start, beta_end))
+    return out
+
+
+def ddim_timesteps(n_steps: int, T: int = 1000) -> np.ndarray:
+    """DDIM timestep sequence, noisiest first (computed by the library)."""
+    out = np.empty(n_steps, dtype=np.int32)
+    _check(lib.cfg_ddim_timesteps(out.ctypes.data_as(POINTER(c_int32)), n_steps, T))
+    return out
+
+
+def sampler_run(x, *, mode: int, n_steps: int, w: float, denoise: Callable, pred_c, pred_u,
+                sched: SchedParams, state, workspace, abar_table: Optional[np.ndarray] = None,
+                timesteps: Optional[np.ndarray] = None, t_grid: Optional[np.ndarray] = None,
+                eta: float = 0.0, seed: int = 0, start_step: int = 0, stream=None) -> None:
+    """Run a whole CFG sampler in the library's host loop (see cfg_sampler_run).
+
+    ``denoise(step, timestep, t)`` must enqueue the two predictions for the
+    current ``x`` into ``pred_c`` / ``pred_u`` on the current stream.  An
+    exception raised by it stops the run and is re-raised here.
+    """
+    _same(x, x, pred_c, pred_u)
+    err = []
+
+    def _cb(user, step, timestep, t, x_t, out_c, out_u, strm):
+        try:
+            denoise(int(step), int(timestep), float(t))
+            return 0
+        except BaseException as e:  # noqa: BLE001 - re-raised after the C loop returns
+            err.append(e)
+            return 1
+
+    cb = DENOISE_FN(_cb)
+    ab = None
+    ts = None
+    tg = None
+    if abar_table is not None:
+        abar_table = np.ascontiguousarray(abar_table, dtype=np.float64)
+        ab = abar_table.ctypes.data_as(POINTER(c_double))
+    if timesteps is not None:
+        timesteps = np.ascontiguousarray(timesteps, dtype=np.int32)
+        ts = timesteps.ctypes.data_as(POINTER(c_int32))
+    if t_grid is not None:
+        t_grid = np.ascontiguousarray(t_grid, dtype=np.float64)
+        tg = t_grid.ctypes.data_as(POINTER(c_double))
+    ws, wsb = _ws(workspace)
+    status = lib.cfg_sampler_run(
+        _dev_ptr(x, "x"), x.numel(), _dtype_code(x), mode, ab,
+        0 if abar_table is None else int(abar_table.shape[0]), ts, tg, n_steps, w, eta, seed, cb,
+        None, _dev_ptr(pred_c, "pred_c"), _dev_ptr(pred_u, "pred_u"), _sp(sched),
+        _dev_ptr(state, "state"), start_step, ws, wsb, _stream(stream))
+    if err:
+        raise err[0]
+    _check(status)

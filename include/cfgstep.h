@@ -1,0 +1,303 @@
+/*
+ * cfgstep.h -- C ABI of the classifier-free-guidance (CFG) sampler step for
+ * one NVIDIA B300 (sm_103a).
+ *
+ * One denoising step of a CFG diffusion sampler, run once per step over the
+ * whole latent, as every multi-GPU scheme on the source pages runs it after
+ * the conditional and unconditional predictions are gathered (xDiT review,
+ * section 3 "CFG Parallelism": the gather happens before the scheduler):
+ *
+ *   1. rel-MAE, the denoising discrepancy between the two predictions
+ *      (Hybridiff notes, "Accelerating Diffusion via Hybrid Data-Pipeline
+ *      Parallelism Based on Conditional Guidance Scheduling", key design 2):
+ *        M_s = sum|p_c - p_u| / sum|p_u|   over the whole latent;
+ *   2. the tau1/tau2 schedule (same notes, key design 3), kept on the device:
+ *        G_s = (M_s - M_{s-L}) / L, tau1' = first s with 0 <= G_s < g_slope,
+ *        tau1 = min(tau1', tau_cap), tau2 = tau1 + k;
+ *   3. guidance  e = p_u + w (p_c - p_u);
+ *   4. the update: DDIM with eta >= 0 (zyxy.net "AIGC text-to-image: how to
+ *      speed up diffusion-model inference", section 3, DDIM sampler), or an
+ *      Euler step of a flow-matching ODE with the velocity pair (Hybridiff
+ *      notes, "Loss / training strategy").
+ *
+ * Conventions for every entry point below:
+ *   - Tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or keeps them.  Parameter structs
+ *     (cfg_sched_params) and tables marked "host" are read on the host
+ *     during the call and not kept.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  All device work is enqueued asynchronously on it; no call
+ *     synchronises the host except where stated.
+ *   - Latents are dense, contiguous arrays of `n` elements in any order the
+ *     caller likes (the step is elementwise apart from the global sums), in
+ *     fp32 (CFG_F32) or bf16 (CFG_BF16).  Arithmetic is fp32; the rel-MAE
+ *     sums are combined in fp64.  16-byte aligned pointers take the 128-bit
+ *     vector path; any other alignment is accepted and takes a scalar path.
+ *   - `x_out` may alias `x_in` (in-place update).
+ *   - Return value: CFG_OK (0) or a negative cfg_status.  On error nothing
+ *     has been enqueued, and cfg_last_error() (per host thread) describes
+ *     the failure.  CFG_ERR_CUDA reports an error returned by the CUDA
+ *     runtime while enqueuing (asynchronous kernel faults surface at the
+ *     caller's next synchronisation, as usual in CUDA).
+ */
+#ifndef CFGSTEP_H
+#define CFGSTEP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define CFG_API __attribute__((visibility("default")))
+#else
+#define CFG_API
+#endif
+
+/* Storage types. */
+enum cfg_dtype { CFG_F32 = 0, CFG_BF16 = 1 };
+
+/* Sampler kinds for cfg_sampler_run. */
+enum cfg_mode { CFG_MODE_DDIM = 0, CFG_MODE_FLOW = 1 };
+
+/* Status codes. */
+enum cfg_status {
+  CFG_OK = 0,
+  CFG_ERR_INVALID_ARG = -1,       /* a pointer, size or parameter is out of range */
+  CFG_ERR_UNSUPPORTED_DTYPE = -2, /* dtype is not CFG_F32 / CFG_BF16 */
+  CFG_ERR_WORKSPACE = -3,         /* workspace missing, too small or misaligned */
+  CFG_ERR_CUDA = -4,              /* the CUDA runtime returned an error */
+  CFG_ERR_CALLBACK = -5           /* the denoiser callback returned non-zero */
+};
+
+/* "Undefined / never" value of the tau fields. */
+#define CFG_TAU_NONE 2147483647
+
+/* Longest run the device-side schedule records. */
+#define CFG_SCHED_MAX_STEPS 1024
+
+/* Phase of a step (Hybridiff notes, "Overall framework"):
+ * Warm-Up [T, tau1], Parallelism (tau1, tau2), Fully-Connecting [tau2, 0],
+ * in step indices: s <= tau1, tau1 < s < tau2, s >= tau2. */
+enum cfg_phase { CFG_PHASE_WARMUP = 0, CFG_PHASE_PARALLEL = 1, CFG_PHASE_FULL = 2 };
+
+/* cfg_sched_state.flags bits. */
+#define CFG_SCHED_FLAG_OUT_OF_ORDER 1u /* a step index arrived that was not n_seen */
+
+/*
+ * Parameters of the tau1/tau2 rule (Hybridiff notes, key design 3).  Host
+ * struct, read during the call.
+ *   L        slope window in steps, >= 1;
+ *   k        tau2 = tau1 + k, >= 0 (the notes' sweet spot is k = 5);
+ *   g_slope  slope threshold, finite;
+ *   tau_cap  >= 0: a calibrated safety cap (the step index of the minimum of
+ *            a previously measured discrepancy curve); -1: the earliest
+ *            argmin of this run's own rel-MAE trace, known after the last step;
+ *   n_steps  steps in the run, 1..CFG_SCHED_MAX_STEPS.
+ * The "t" of the notes' rule is read as the step index s, counted from the
+ * first denoising step (s = 0 at the noisiest timestep).
+ */
+typedef struct cfg_sched_params {
+  int32_t L;
+  int32_t k;
+  double g_slope;
+  int32_t tau_cap;
+  int32_t n_steps;
+} cfg_sched_params;
+
+/*
+ * Device-resident schedule state, one per sampler run (caller-allocated
+ * device memory of sizeof(cfg_sched_state) bytes, 8-byte aligned; contents
+ * need no initialisation: step 0 resets it).  Updated by one device thread
+ * after each step's rel-MAE is known; the host reads it whenever it likes.
+ *   n_seen      steps recorded (the next expected step index);
+ *   tau1p       tau1' (CFG_TAU_NONE until found);
+ *   argmin      earliest index of the smallest non-NaN M so far (-1: none);
+ *   tau_cap     the cap used (CFG_TAU_NONE until decided);
+ *   tau1, tau2  CFG_TAU_NONE until decided;
+ *   decided_at  step at which tau1/tau2 became final (-1 before): with a
+ *               calibrated cap, min(tau1', tau_cap); otherwise the last step;
+ *   flags       CFG_SCHED_FLAG_* bits;
+ *   min_M       the smallest M so far;
+ *   M[s]        rel-MAE trace; G[s] slope (NaN for s < L);
+ *   phase[s]    cfg_phase of each step, written at the last step.
+ * NaN compares false everywhere (a NaN M never sets tau1' or the argmin).
+ */
+typedef struct cfg_sched_state {
+  int32_t n_seen;
+  int32_t tau1p;
+  int32_t argmin;
+  int32_t tau_cap;
+  int32_t tau1;
+  int32_t tau2;
+  int32_t decided_at;
+  uint32_t flags;
+  double min_M;
+  double M[CFG_SCHED_MAX_STEPS];
+  double G[CFG_SCHED_MAX_STEPS];
+  uint8_t phase[CFG_SCHED_MAX_STEPS];
+} cfg_sched_state;
+
+/*
+ * Bytes of device workspace a step or reduction over `n` elements of
+ * `dtype` needs (the per-block partial sums of the rel-MAE reduction and a
+ * completion counter).  The value does not depend on the device.  Returns 0
+ * for an unsupported dtype or n < 0.
+ */
+CFG_API size_t cfg_workspace_bytes(int64_t n, int32_t dtype);
+
+/*
+ * Prepare a workspace for first use: zero its completion counter on
+ * `stream`.  Call once per workspace buffer (a zero-filled buffer is
+ * already prepared); every later call leaves the counter at zero again.
+ * ws: device, 16-byte aligned, ws_bytes >= cfg_workspace_bytes(...).
+ * One workspace must not be used by two calls that may run concurrently.
+ */
+CFG_API int cfg_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * rel-MAE alone (Hybridiff notes, key design 2; with the velocity pair for
+ * flow models, "Loss / training strategy"):
+ *   M = sum_i |pred_c[i] - pred_u[i]| / sum_i |pred_u[i]|
+ * with 0/0 -> 0 and x/0 -> +inf.
+ *   pred_c, pred_u  device, n elements of dtype;
+ *   M_out           device double, nullable: receives M;
+ *   st, sp          nullable together: when given, M is recorded as step
+ *                   `step` of the schedule (0 <= step < sp->n_steps);
+ *   ws, ws_bytes    device workspace (cfg_workspace_bytes, cfg_workspace_init).
+ * Reads 2n elements; one fused pass plus an in-kernel fixed-order fp64
+ * combine of the block partials (deterministic for a given device).
+ */
+CFG_API int cfg_relmae_reduce(const void* pred_c, const void* pred_u, int64_t n, int32_t dtype,
+                              double* M_out, cfg_sched_state* st, const cfg_sched_params* sp,
+                              int32_t step, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * One fused CFG + DDIM step (zyxy.net DDIM sampler, section 3):
+ *   e      = pred_u + w (pred_c - pred_u)
+ *   sigma  = eta sqrt((1 - abar_prev)/(1 - abar_t) (1 - abar_t/abar_prev))
+ *   x0     = (x - sqrt(1 - abar_t) e) / sqrt(abar_t)
+ *   x_out  = sqrt(abar_prev) x0 + sqrt(1 - abar_prev - sigma^2) e + sigma z
+ * abar_prev = 1 makes this the last step (x_out = x0).  z ~ N(0,1) is drawn
+ * in registers from Philox4x32-10 with key = seed and counter
+ * (i/4 low word, i/4 high word, step, 0) and Box-Muller on 23-bit uniforms
+ * (see cfg_randn), so it costs no memory traffic and is reproducible.
+ * Fused with the rel-MAE of (pred_c, pred_u) and, when st is given, the
+ * schedule update for step `step`: one pass reading x, pred_c, pred_u and
+ * writing x_out (4n elements of traffic).
+ *   x_out, x_in     device, n elements of dtype (may alias);
+ *   pred_c, pred_u  device, n elements of dtype (epsilon predictions);
+ *   w               finite guidance scale;
+ *   abar_t          in (0, 1); abar_prev in (0, 1], with the DDIM radicands
+ *                   non-negative for the given eta (else CFG_ERR_INVALID_ARG);
+ *   eta             >= 0, finite;
+ *   seed, step      Philox key and counter word (step >= 0);
+ *   M_out           device double, nullable;  st, sp: see cfg_relmae_reduce.
+ * Arithmetic: fp32 for bf16 storage; for fp32 storage, compensated
+ * (double-fp32) arithmetic so the stored result is the fp32 rounding of the
+ * exact step in all but rare near-tie cases.  The coefficients are formed
+ * in fp64 on the host.
+ */
+CFG_API int cfg_ddim_step(void* x_out, const void* x_in, const void* pred_c, const void* pred_u,
+                          int64_t n, int32_t dtype, float w, double abar_t, double abar_prev,
+                          float eta, uint64_t seed, int32_t step, double* M_out,
+                          cfg_sched_state* st, const cfg_sched_params* sp, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/*
+ * One fused CFG + Euler flow step (flow matching, Hybridiff notes "Loss /
+ * training strategy": rel-MAE on the velocity pair):
+ *   v     = v_u + w (v_c - v_u)
+ *   x_out = x + (t_next - t_cur) v
+ * with the same fused rel-MAE / schedule handling and arguments as
+ * cfg_ddim_step (t_cur, t_next finite; the convention x_t = (1-t) x_0 + t x_1,
+ * v = x_1 - x_0, integrates from t = 1 to t = 0).
+ */
+CFG_API int cfg_flow_step(void* x_out, const void* x_in, const void* v_c, const void* v_u,
+                          int64_t n, int32_t dtype, float w, double t_cur, double t_next,
+                          int32_t step, double* M_out, cfg_sched_state* st,
+                          const cfg_sched_params* sp, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Record an externally computed rel-MAE value M as step `step` of the
+ * schedule (for callers that reduce the discrepancy elsewhere, e.g. from
+ * partial sums of a latent split across devices).  Enqueues one tiny
+ * kernel on `stream`.  st: device; sp: host (as cfg_relmae_reduce).
+ */
+CFG_API int cfg_sched_observe(cfg_sched_state* st, const cfg_sched_params* sp, int32_t step,
+                              double M, void* stream);
+
+/*
+ * Denoiser callback of cfg_sampler_run: must enqueue on `stream` the two
+ * predictions for x_t into pred_c / pred_u (n elements of the run's dtype)
+ * and return 0, or return non-zero to stop the run (cfg_sampler_run then
+ * returns CFG_ERR_CALLBACK).  For DDIM, `timestep` is the training timestep
+ * and `t` its abar; for flow, `timestep` is the step index and `t` the time.
+ */
+typedef int32_t (*cfg_denoise_fn)(void* user, int32_t step, int32_t timestep, double t,
+                                  const void* x_t, void* pred_c, void* pred_u, void* stream);
+
+/*
+ * A whole CFG sampler run, host loop over steps start_step .. n_steps-1:
+ * the callback fills the predictions, then the fused step updates x in
+ * place and the schedule on the device.  No host synchronisation inside.
+ *   x                      device, n elements: x_T in, x_0 out;
+ *   mode                   CFG_MODE_DDIM or CFG_MODE_FLOW;
+ *   abar_table, T          DDIM: host table of abar over T training steps;
+ *   timesteps              DDIM: host, n_steps entries in [0, T), the
+ *                          timestep of each step, noisiest first (see
+ *                          cfg_ddim_timesteps); the step after the last uses
+ *                          abar = 1 (the last step returns x0);
+ *   t_grid                 FLOW: host, n_steps + 1 times, or NULL for the
+ *                          uniform grid t_s = 1 - s/n_steps;
+ *   w, eta, seed           as cfg_ddim_step (eta unused for FLOW);
+ *   fn, user               denoiser callback;
+ *   pred_c_buf, pred_u_buf device, n elements each, filled by the callback;
+ *   sp, st                 schedule (both required; sp->n_steps == n_steps);
+ *   start_step             first step to run (resume from a saved x and st);
+ *   ws, ws_bytes           workspace for n elements.
+ */
+CFG_API int cfg_sampler_run(void* x, int64_t n, int32_t dtype, int32_t mode,
+                            const double* abar_table, int32_t T, const int32_t* timesteps,
+                            const double* t_grid, int32_t n_steps, float w, float eta,
+                            uint64_t seed, cfg_denoise_fn fn, void* user, void* pred_c_buf,
+                            void* pred_u_buf, const cfg_sched_params* sp, cfg_sched_state* st,
+                            int32_t start_step, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Standard normal noise, the same stream the DDIM step draws for eta > 0:
+ * out[i] = Box-Muller normal of element i from Philox4x32-10 with key
+ * (seed low word, seed high word) and counter (i/4 low, i/4 high, step,
+ * stream_id); words (0,1) give elements 4q, 4q+1 as (rho cos, rho sin) with
+ * rho = sqrt(-2 ln u0), angle 2 pi u1; words (2,3) likewise give 4q+2, 4q+3;
+ * u = (2 (r >> 9) + 1) / 2^24.  The DDIM step uses stream_id 0.
+ *   out: device float, n elements (n >= 0).
+ */
+CFG_API int cfg_randn(float* out, int64_t n, uint64_t seed, uint32_t step, uint32_t stream_id,
+                      void* stream);
+
+/*
+ * Host helpers (no device work).
+ * cfg_abar_linear: abar[t] = prod_{i<=t} (1 - beta_i), beta linear from
+ *   beta_start to beta_end over T steps, sequential fp64 product.
+ *   abar_out: host, T doubles; T >= 1; 0 <= beta_start, beta_end < 1.
+ * cfg_ddim_timesteps: the DDIM timestep sequence of the zyxy.net sampler,
+ *   round(linspace(0, T-1, n_steps)) walked from the largest down
+ *   (ties to even).  out: host, n_steps int32; 1 <= n_steps <= T.
+ */
+CFG_API int cfg_abar_linear(double* abar_out, int32_t T, double beta_start, double beta_end);
+CFG_API int cfg_ddim_timesteps(int32_t* out, int32_t n_steps, int32_t T);
+
+/* Message of the last failed call on this host thread ("" if none). */
+CFG_API const char* cfg_last_error(void);
+
+/* Library version string. */
+CFG_API const char* cfg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CFGSTEP_H */

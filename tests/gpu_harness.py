@@ -1,0 +1,149 @@
+"""GPU-side harness for the parity tests: the synthetic denoisers on the device.
+
+The denoisers stand in for the model; they are not part of the sampler step.
+They follow the same definition as the oracle's (``oracle.cfg_oracle.gaussian_eps``
+/ ``flow_velocity``): evaluate in float64 one operation at a time
+(``(x - sa*mean) * A (+ perturbation)``, or ``(x - mean) * (1/t)``), round to
+fp32, then to the storage type -- so, given the same stored ``x``, both sides
+store the same prediction bits.  Implemented here independently with torch
+float64 device ops (each op a separate IEEE-rounded kernel, no fusion).
+The sampler step itself always runs in the library (``cfg_sampler_run``).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import Dict, Optional
+
+import numpy as np
+import torch
+
+import cfg_guided_sampler_step_b300 as cs
+import workloads as W
+
+TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def to_device_stored(a: np.ndarray, dtype: str, device) -> torch.Tensor:
+    """Upload a stored array (float32, or bf16 bits as uint16) as a tensor of the storage dtype."""
+    if dtype == "f32":
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
+    bits = np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)
+    return torch.from_numpy(bits).to(device).view(torch.bfloat16)
+
+
+def to_host_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64).reshape(-1)
+
+
+class Denoiser:
+    """Synthetic CFG denoiser of a workload on the device (fills pred_c / pred_u)."""
+
+    def __init__(self, wl: W.Workload, inputs: Dict[str, np.ndarray], x: torch.Tensor,
+                 pred_c: torch.Tensor, pred_u: torch.Tensor):
+        self.wl = wl
+        dev = x.device
+        reps = wl.n // int(np.prod(wl.mean_shape))
+        self.mc = torch.from_numpy(np.tile(inputs["mean_c"].reshape(-1), reps).astype(np.float64)).to(dev)
+        self.mu = torch.from_numpy(np.tile(inputs["mean_u"].reshape(-1), reps).astype(np.float64)).to(dev)
+        self.x, self.pc, self.pu = x, pred_c, pred_u
+        self.calls = 0
+
+    def _store(self, t64: torch.Tensor, out: torch.Tensor) -> None:
+        out.view(-1).copy_(t64.to(torch.float32).to(out.dtype))
+
+    def _perturb(self, step: int, branch: str) -> Optional[torch.Tensor]:
+        p = W.draw_perturbation(self.wl, step, branch)
+        if p is None:
+            return None
+        return torch.from_numpy(p.astype(np.float64)).to(self.x.device)
+
+    def __call__(self, step: int, timestep: int, t: float) -> None:
+        self.calls += 1
+        wl = self.wl
+        x64 = self.x.view(-1).to(torch.float64)
+        if wl.mode == "ddim":
+            abar = t
+            sa = math.sqrt(abar)
+            A = math.sqrt(1.0 - abar) / (abar * wl.data_std * wl.data_std + (1.0 - abar))
+            for mean, out, br in ((self.mc, self.pc, "c"), (self.mu, self.pu, "u")):
+                v = mean * sa
+                v = x64 - v
+                v = v * A
+                p = self._perturb(step, br)
+                if p is not None:
+                    v = v + p
+                self._store(v, out)
+        else:
+            inv_t = 1.0 / t
+            for mean, out in ((self.mc, self.pc), (self.mu, self.pu)):
+                v = x64 - mean
+                v = v * inv_t
+                self._store(v, out)
+
+
+@dataclass
+class GpuRun:
+    x0: np.ndarray
+    state: Dict[str, object]
+
+
+def run_workload(wl: W.Workload, inputs: Dict[str, np.ndarray], device="cuda",
+                 start_from: Optional[tuple] = None, stop_after: Optional[int] = None) -> GpuRun:
+    """The whole sampler of a workload through cfg_sampler_run, with the device denoiser."""
+    x = to_device_stored(inputs["x_T"], wl.dtype, device)
+    pc = torch.empty_like(x)
+    pu = torch.empty_like(x)
+    ws = cs.new_workspace(wl.n, cs.CFG_F32 if wl.dtype == "f32" else cs.CFG_BF16, device)
+    st = cs.new_sched_state(device)
+    start = 0
+    if start_from is not None:
+        x0_saved, st_saved, start = start_from
+        x.copy_(x0_saved)
+        st.copy_(st_saved)
+    sp = cs.SchedParams(n_steps=wl.n_steps, L=wl.L, g_slope=wl.g_slope, k=wl.k, tau_cap=wl.tau_cap)
+    den = Denoiser(wl, inputs, x, pc, pu)
+    kw = dict(mode=cs.CFG_MODE_DDIM if wl.mode == "ddim" else cs.CFG_MODE_FLOW,
+              n_steps=wl.n_steps, w=wl.w, denoise=den, pred_c=pc, pred_u=pu, sched=sp, state=st,
+              workspace=ws, eta=wl.eta, seed=wl.seed, start_step=start)
+    if wl.mode == "ddim":
+        kw["abar_table"] = cs.abar_linear(wl.T, wl.beta_start, wl.beta_end)
+        kw["timesteps"] = cs.ddim_timesteps(wl.n_steps, wl.T)
+    if stop_after is not None:
+        # run only steps [start, stop_after): emulate an interrupted run
+        n_total = wl.n_steps
+
+        def den_stop(step, timestep, t):
+            if step >= stop_after:
+                raise StopIteration(step)
+            den(step, timestep, t)
+        kw["denoise"] = den_stop
+        try:
+            cs.sampler_run(x, **kw)
+        except StopIteration:
+            pass
+        torch.cuda.synchronize()
+        assert n_total == wl.n_steps
+        return GpuRun(to_host_f64(x), {"x": x.clone(), "st": st.clone()})
+    cs.sampler_run(x, **kw)
+    torch.cuda.synchronize()
+    return GpuRun(to_host_f64(x), cs.read_sched_state(st))
+
+
+def rel_err(got: np.ndarray, ref: np.ndarray) -> float:
+    """max_i |got - ref| / max(|ref|, 1)."""
+    if got.size == 0:
+        return 0.0
+    return float(np.max(np.abs(got - ref) / np.maximum(np.abs(ref), 1.0)))
+
+
+def ulp_distance_f32(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    ia = np.asarray(a, dtype=np.float32).view(np.int32).astype(np.int64)
+    ib = np.asarray(b, dtype=np.float32).view(np.int32).astype(np.int64)
+    ia = np.where(ia < 0, -(ia & 0x7FFFFFFF), ia)
+    ib = np.where(ib < 0, -(ib & 0x7FFFFFFF), ib)
+    return np.abs(ia - ib)
+
+
+def ulp_distance_bf16(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    return ulp_distance_f32(a, b) >> 16

@@ -1,0 +1,290 @@
+"""Single-call parity of the CUDA library against the CPU oracle (needs a GPU).
+
+Every call goes through the C ABI (via the ctypes binding) on stored inputs
+drawn by ``workloads``; the oracle computes the same step in float64 on the
+same stored values.  Tolerances:
+
+* fp32 storage: max abs error <= 1e-5, and for eta = 0 every element within
+  1 ulp of the oracle's rounded value (the library uses compensated
+  arithmetic for fp32 storage); with eta > 0 the noise itself is an fp32
+  Box-Muller value (relative error ~4e-7), so only the 1e-5 bound applies;
+* bf16 storage: max |g - o| / max(|o|, 1) <= 2e-2, and every element within
+  1 bf16 ulp (fp32 arithmetic, one final rounding) unless cancellation left
+  a result below the fp32 arithmetic's absolute error;
+* rel-MAE: relative error <= 1e-6 (fp32 L1 partial sums with Kahan
+  compensation, fp64 combine).
+"""
+import json
+import math
+from pathlib import Path
+
+import numpy as np
+import pytest
+import torch
+
+import cfg_guided_sampler_step_b300 as cs
+import workloads as W
+from oracle import cfg_oracle as O
+from gpu_harness import TORCH_DTYPE, rel_err, to_device_stored, to_host_f64, ulp_distance_bf16, ulp_distance_f32
+
+pytestmark = pytest.mark.gpu
+GOLDEN = Path(__file__).parent / "golden"
+
+SIZES = [0, 1, 7, 9, 4097, 65536 + 3, 1 << 20, 3 * (1 << 20) + 5]
+
+
+def _code(dtype):
+    return cs.CFG_F32 if dtype == "f32" else cs.CFG_BF16
+
+
+def _inputs(n, dtype, seed, cuda, offset=0):
+    """Stored x, pred_c, pred_u on the device (optionally starting `offset` elements into
+    their allocation, so the pointers are not 16-byte aligned) and their exact fp64 values."""
+    d = W.draw_prediction_pair(n, dtype, seed)
+    out = {}
+    for k in ("x", "c", "u"):
+        arr = d[k]
+        if offset:
+            full = to_device_stored(np.concatenate([np.zeros(offset, dtype=arr.dtype), arr]), dtype,
+                                    cuda)
+            out[k] = full[offset:]
+        else:
+            out[k] = to_device_stored(arr, dtype, cuda)
+        out[k + "64"] = W.stored_to_f64(arr, dtype)
+    return out
+
+
+def _compare(got, ref, dtype, strict_ulp):
+    """Stated tolerance, plus (strict_ulp) every element within 1 ulp of the oracle's stored
+    value or, where the result is tiny after cancellation, within the arithmetic's absolute
+    error bound (fp32 arithmetic: 3 * 2^-24 * |terms| <= 2^-17 for |terms| <= 20;
+    compensated fp32: <= 1e-9)."""
+    if got.size == 0:
+        return
+    diff = np.abs(got - ref)
+    if dtype == "f32":
+        assert float(diff.max()) <= 1e-5, float(diff.max())
+        if strict_ulp:
+            ok = (ulp_distance_f32(got, ref) <= 1) | (diff <= 1e-9)
+            assert ok.all(), np.flatnonzero(~ok)[:10]
+    else:
+        assert rel_err(got, ref) <= 2e-2
+        if strict_ulp:
+            ok = (ulp_distance_bf16(got, ref) <= 1) | (diff <= 2.0**-17)
+            assert ok.all(), np.flatnonzero(~ok)[:10]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("n", SIZES)
+@pytest.mark.parametrize("eta", [0.0, 1.0])
+def test_ddim_step_matches_oracle(cuda, dtype, n, eta):
+    d = _inputs(n, dtype, seed=100 + n % 97, cuda=cuda)
+    abar = O.abar_linear()
+    ab, abp = float(abar[500]), float(abar[480])
+    w, seed, step = 7.5, 0xC0FFEE_1234, 17
+    x_out = torch.empty_like(d["x"])
+    M = torch.zeros(1, dtype=torch.float64, device=cuda)
+    ws = cs.new_workspace(n, _code(dtype), cuda)
+    cs.ddim_step(x_out, d["x"], d["c"], d["u"], w=w, abar_t=ab, abar_prev=abp, eta=eta, seed=seed,
+                 step=step, M_out=M, workspace=ws)
+    torch.cuda.synchronize()
+    ref, refM = O.ddim_step(d["x64"], d["c64"], d["u64"], dtype, w, ab, abp, eta, seed, step)
+    _compare(to_host_f64(x_out), ref, dtype, strict_ulp=(eta == 0.0))
+    gotM = float(M.item())
+    if n == 0:
+        assert gotM == 0.0 and refM == 0.0
+    else:
+        assert abs(gotM - refM) <= 1e-6 * refM
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("n", [1, 9, 4097, 1 << 20])
+def test_ddim_last_step_and_in_place(cuda, dtype, n):
+    """abar_prev = 1 returns the x0 prediction; x_out may alias x_in."""
+    d = _inputs(n, dtype, seed=7, cuda=cuda)
+    ab = float(O.abar_linear()[0])
+    ws = cs.new_workspace(n, _code(dtype), cuda)
+    x = d["x"].clone()
+    cs.ddim_step(x, x, d["c"], d["u"], w=6.0, abar_t=ab, abar_prev=1.0, eta=1.0, seed=3, step=49,
+                 workspace=ws)
+    torch.cuda.synchronize()
+    ref, _ = O.ddim_step(d["x64"], d["c64"], d["u64"], dtype, 6.0, ab, 1.0, 1.0, 3, 49, last=True)
+    _compare(to_host_f64(x), ref, dtype, strict_ulp=True)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("offset", [1, 3])
+def test_misaligned_pointers_take_the_scalar_path(cuda, dtype, offset):
+    n = 50_000 + 3
+    d = _inputs(n, dtype, seed=11, cuda=cuda, offset=offset)
+    assert d["x"].data_ptr() % 16 != 0
+    abar = O.abar_linear()
+    ab, abp = float(abar[700]), float(abar[680])
+    x_out = torch.empty(n + 1, dtype=TORCH_DTYPE[dtype], device=cuda)[1:]
+    M = torch.zeros(1, dtype=torch.float64, device=cuda)
+    ws = cs.new_workspace(n, _code(dtype), cuda)
+    cs.ddim_step(x_out, d["x"], d["c"], d["u"], w=5.0, abar_t=ab, abar_prev=abp, eta=1.0, seed=5,
+                 step=2, M_out=M, workspace=ws)
+    torch.cuda.synchronize()
+    ref, refM = O.ddim_step(d["x64"], d["c64"], d["u64"], dtype, 5.0, ab, abp, 1.0, 5, 2)
+    _compare(to_host_f64(x_out), ref, dtype, strict_ulp=False)
+    assert abs(M.item() - refM) <= 1e-6 * refM
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("n", [0, 1, 9, 4097, 1 << 20, 3 * (1 << 20) + 5])
+def test_flow_step_matches_oracle(cuda, dtype, n):
+    d = _inputs(n, dtype, seed=200 + n % 13, cuda=cuda)
+    t_cur, t_next = 1.0 - 3 / 28, 1.0 - 4 / 28
+    x_out = torch.empty_like(d["x"])
+    M = torch.zeros(1, dtype=torch.float64, device=cuda)
+    ws = cs.new_workspace(n, _code(dtype), cuda)
+    cs.flow_step(x_out, d["x"], d["c"], d["u"], w=3.5, t_cur=t_cur, t_next=t_next, M_out=M,
+                 workspace=ws)
+    torch.cuda.synchronize()
+    ref, refM = O.flow_step(d["x64"], d["c64"], d["u64"], dtype, 3.5, t_cur, t_next)
+    _compare(to_host_f64(x_out), ref, dtype, strict_ulp=True)
+    if n:
+        assert abs(M.item() - refM) <= 1e-6 * refM
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("n", [0, 1, 7, 4097, 1 << 20])
+def test_relmae_reduce_matches_oracle(cuda, dtype, n):
+    d = _inputs(n, dtype, seed=300 + n % 7, cuda=cuda)
+    M = torch.full((1,), -1.0, dtype=torch.float64, device=cuda)
+    ws = cs.new_workspace(n, _code(dtype), cuda)
+    cs.relmae_reduce(d["c"], d["u"], M_out=M, workspace=ws)
+    torch.cuda.synchronize()
+    refM = O.rel_mae(d["c64"], d["u64"])
+    if n == 0:
+        assert M.item() == 0.0
+    else:
+        assert abs(M.item() - refM) <= 1e-6 * refM
+
+
+def test_relmae_degenerate_cases(cuda):
+    ws = cs.new_workspace(64, cs.CFG_F32, cuda)
+    M = torch.zeros(1, dtype=torch.float64, device=cuda)
+    z = torch.zeros(64, device=cuda)
+    one = torch.ones(64, device=cuda)
+    cs.relmae_reduce(z, z, M_out=M, workspace=ws)
+    assert M.item() == 0.0
+    cs.relmae_reduce(one, z, M_out=M, workspace=ws)
+    assert M.item() == math.inf
+    cs.relmae_reduce(one, one, M_out=M, workspace=ws)
+    assert M.item() == 0.0
+    nan = one.clone()
+    nan[5] = float("nan")
+    cs.relmae_reduce(nan, one, M_out=M, workspace=ws)
+    assert math.isnan(M.item())
+
+
+def test_identical_branches_ignore_w(cuda):
+    n = 10_001
+    d = _inputs(n, "bf16", seed=13, cuda=cuda)
+    ab, abp = float(O.abar_linear()[300]), float(O.abar_linear()[280])
+    ws = cs.new_workspace(n, cs.CFG_BF16, cuda)
+    outs = []
+    for w in (0.0, 1.0, 7.5):
+        o = torch.empty_like(d["x"])
+        M = torch.zeros(1, dtype=torch.float64, device=cuda)
+        cs.ddim_step(o, d["x"], d["u"], d["u"], w=w, abar_t=ab, abar_prev=abp, M_out=M, workspace=ws)
+        torch.cuda.synchronize()
+        assert M.item() == 0.0
+        outs.append(o)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+def test_step_is_deterministic(cuda):
+    n = 3 * (1 << 20) + 5
+    d = _inputs(n, "bf16", seed=17, cuda=cuda)
+    ab, abp = float(O.abar_linear()[600]), float(O.abar_linear()[580])
+    ws = cs.new_workspace(n, cs.CFG_BF16, cuda)
+    res = []
+    for _ in range(2):
+        o = torch.empty_like(d["x"])
+        M = torch.zeros(1, dtype=torch.float64, device=cuda)
+        cs.ddim_step(o, d["x"], d["c"], d["u"], w=7.5, abar_t=ab, abar_prev=abp, eta=1.0, seed=1,
+                     step=3, M_out=M, workspace=ws)
+        torch.cuda.synchronize()
+        res.append((o.clone(), M.item()))
+    assert torch.equal(res[0][0], res[1][0])
+    assert res[0][1] == res[1][1]
+
+
+# ---------------------------------------------------------------------------
+# Noise stream
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("n,seed,step,stream", [
+    (1, 0, 0, 0), (7, 2, 5, 0), (4099, 0x123456789ABCDEF, 17, 0), (1 << 20, 2, 49, 3)])
+def test_randn_matches_oracle(cuda, n, seed, step, stream):
+    """The integer Philox stream is shared exactly (any word error moves z by O(1));
+    the fp32 Box-Muller value is within 4 fp32 ulps of the fp64 one."""
+    out = torch.empty(n, dtype=torch.float32, device=cuda)
+    cs.randn(out, seed=seed, step=step, stream_id=stream)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    ref = O.gaussian_noise(n, seed, step, stream)
+    err = np.abs(got - ref) / np.maximum(np.abs(ref), 1.0)
+    assert err.max() <= 4 * 2.0**-23, err.max()
+
+
+def test_randn_misaligned_output(cuda):
+    n = 1001
+    buf = torch.empty(n + 1, dtype=torch.float32, device=cuda)
+    cs.randn(buf[1:], seed=4, step=1)
+    torch.cuda.synchronize()
+    ref = O.gaussian_noise(n, 4, 1)
+    assert np.max(np.abs(buf[1:].cpu().numpy() - ref)) <= 4 * 2.0**-23 * 6
+
+
+# ---------------------------------------------------------------------------
+# Schedule rule on the device
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("case", json.loads((GOLDEN / "schedule_traces.json").read_text())["traces"],
+                         ids=lambda c: c["name"])
+def test_schedule_golden_on_device(cuda, case):
+    M = [math.nan if v == "nan" else float(v) for v in case["M"]]
+    st = cs.new_sched_state(cuda)
+    sp = cs.SchedParams(n_steps=len(M), L=case["L"], g_slope=case["g_slope"], k=case["k"],
+                        tau_cap=case["tau_cap"])
+    for s, m in enumerate(M):
+        cs.sched_observe(st, sp, s, m)
+    got = cs.read_sched_state(st)
+    for key, val in case["expect"].items():
+        assert got[key] == val, (key, got[key], val)
+    assert list(got["phase"]) == case["phase"]
+    ref = O.schedule(np.array(M), case["L"], case["g_slope"], case["k"], case["tau_cap"])
+    assert np.array_equal(got["G"], ref.G, equal_nan=True)
+    assert got["flags"] == 0 and got["n_seen"] == len(M)
+
+
+def test_schedule_random_traces_match_oracle(cuda):
+    g = np.random.default_rng(21)
+    for trial in range(20):
+        N = int(g.integers(1, 80))
+        M = np.abs(np.cumsum(g.standard_normal(N) * 0.01)) + 0.05
+        L = int(g.integers(1, 8))
+        gs = float(g.choice([1e-3, 5e-3, 0.0, 1.0]))
+        k = int(g.integers(0, 20))
+        cap = int(g.choice([-1, -1, int(g.integers(0, 100))]))
+        st = cs.new_sched_state(cuda)
+        sp = cs.SchedParams(n_steps=N, L=L, g_slope=gs, k=k, tau_cap=cap)
+        for s in range(N):
+            cs.sched_observe(st, sp, s, float(M[s]))
+        got = cs.read_sched_state(st)
+        ref = O.schedule(M, L, gs, k, cap)
+        assert {k_: got[k_] for k_ in ref.as_dict()} == ref.as_dict(), trial
+        assert np.array_equal(got["phase"], ref.phase)
+
+
+def test_schedule_flags_out_of_order(cuda):
+    st = cs.new_sched_state(cuda)
+    sp = cs.SchedParams(n_steps=10)
+    cs.sched_observe(st, sp, 0, 1.0)
+    cs.sched_observe(st, sp, 2, 1.0)
+    got = cs.read_sched_state(st)
+    assert got["flags"] & 1
+    cs.sched_observe(st, sp, 0, 1.0)      # step 0 starts a new run
+    assert cs.read_sched_state(st)["flags"] == 0
