@@ -234,17 +234,23 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
     props = torch.cuda.get_device_properties(device)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2**20))
     set_bytes = 4 * wl.n * wl.elem_bytes          # x_in, pred_c, pred_u, x_out
+    # enough sets for 4x the L2, rounded up to whole sampler runs
     n_sets = max(2, math.ceil(4 * l2 / set_bytes))
+    n_sets = wl.n_steps * math.ceil(n_sets / wl.n_steps)
     sets = make_sets(wl, n_sets, device, torch)
     code = cs.CFG_F32 if wl.dtype == "f32" else cs.CFG_BF16
     ws = cs.new_workspace(wl.n, code, device)
     st = cs.new_sched_state(device)
-    sp = cs.SchedParams(n_steps=wl.n_steps, L=wl.L, g_slope=wl.g_slope, k=wl.k, tau_cap=wl.tau_cap)
+    # as in a sampler run: each step's reduction is completed by the next step's launch
+    sp = cs.SchedParams(n_steps=wl.n_steps, L=wl.L, g_slope=wl.g_slope, k=wl.k, tau_cap=wl.tau_cap,
+                        defer=True)
     plan = step_plan(wl, cs)
     # graph step j uses buffer set j % n_sets (read x_in, pred_c, pred_u; write x_out) and
-    # sampler step j % N.  A graph is a whole number of rotations, so a set is reused only
-    # after every other set has passed (>= 4x L2 of traffic in between).
-    G = n_sets * max(1, round(4 * max(n_sets, wl.n_steps) / n_sets))
+    # sampler step j % N.  A graph is one rotation over the sets = whole sampler runs, so a
+    # set is reused only after every other set has passed (>= 4x L2 of traffic in between)
+    # and every replay ends on a run's last step (which finishes its reduction in-launch).
+    # A graph of a partial run ends with a workspace flush, so no step's work is left over.
+    G = n_sets
 
     def capture(count):
         g = torch.cuda.CUDAGraph()
@@ -253,11 +259,14 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
         with torch.cuda.stream(s):
             for j in range(min(count, 8)):          # eager warm-up of the launch path
                 enqueue_step(cs, wl, sets[j % n_sets], plan[j % wl.n_steps], ws, st, sp)
+            cs.workspace_flush(ws)
         torch.cuda.current_stream(device).wait_stream(s)
         torch.cuda.synchronize(device)
         with torch.cuda.graph(g, stream=s):
             for j in range(count):
                 enqueue_step(cs, wl, sets[j % n_sets], plan[j % wl.n_steps], ws, st, sp)
+            if count % wl.n_steps:
+                cs.workspace_flush(ws)
         torch.cuda.synchronize(device)
         return g
 
@@ -295,7 +304,8 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
     ms = start.elapsed_time(end)
     state = cs.read_sched_state(st)
     return {"ms": ms, "n_sets": n_sets, "set_bytes": set_bytes, "l2_bytes": l2,
-            "graph_steps": G, "launches": steps, "state_flags": state["flags"]}
+            "graph_steps": G, "launches": steps + (1 if steps % wl.n_steps else 0),
+            "state_flags": state["flags"]}
 
 
 def time_e2e(wl: W.Workload, steps: int, device):
@@ -318,7 +328,9 @@ def time_e2e(wl: W.Workload, steps: int, device):
     dM = torch.zeros(1, dtype=torch.float64, device=device)
     ws = cs.new_workspace(wl.n, cs.CFG_F32 if wl.dtype == "f32" else cs.CFG_BF16, device)
     st = cs.new_sched_state(device)
-    sp = cs.SchedParams(n_steps=wl.n_steps, L=wl.L, g_slope=wl.g_slope, k=wl.k, tau_cap=wl.tau_cap)
+    # every step finishes its own reduction, so each step's M is complete when read back
+    sp = cs.SchedParams(n_steps=wl.n_steps, L=wl.L, g_slope=wl.g_slope, k=wl.k, tau_cap=wl.tau_cap,
+                        defer=False)
     plan = step_plan(wl, cs)
 
     def one(i):
@@ -493,7 +505,7 @@ def main(argv=None):
                      "frac_of_8tbs_spec": achieved / 8000.0},
         "e2e": {"value": e2e_v, "unit": e2e["unit"], "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
                 "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]},
-        "gpu_launches": args.steps,
+        "gpu_launches": dev["launches"],
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -23,11 +23,13 @@ import numpy as np
 __all__ = [
     "CFG_F32", "CFG_BF16", "CFG_MODE_DDIM", "CFG_MODE_FLOW", "TAU_NONE", "SCHED_MAX_STEPS",
     "CfgError", "SchedParams", "lib", "lib_path", "workspace_bytes", "new_workspace",
-    "new_sched_state", "read_sched_state", "relmae_reduce", "ddim_step", "flow_step",
+    "new_sched_state", "read_sched_state", "workspace_flush", "SCHED_DEFER", "relmae_reduce", "ddim_step", "flow_step",
     "sched_observe", "randn", "abar_linear", "ddim_timesteps", "sampler_run", "version",
 ]
 
 CFG_F32, CFG_BF16 = 0, 1
+SCHED_DEFER = 1
+SCHED_FLAG_OUT_OF_ORDER, SCHED_FLAG_DEFER_CLASH = 1, 2
 CFG_MODE_DDIM, CFG_MODE_FLOW = 0, 1
 TAU_NONE = 2**31 - 1
 SCHED_MAX_STEPS = 1024
@@ -47,7 +49,7 @@ class CfgError(RuntimeError):
 
 class SchedParamsC(Structure):
     _fields_ = [("L", c_int32), ("k", c_int32), ("g_slope", c_double), ("tau_cap", c_int32),
-                ("n_steps", c_int32)]
+                ("n_steps", c_int32), ("flags", c_uint32), ("reserved", c_int32)]
 
 
 class SchedStateC(Structure):
@@ -73,6 +75,7 @@ def _load() -> ctypes.CDLL:
         "cfg_version": (c_char_p, []),
         "cfg_workspace_bytes": (c_size_t, [c_int64, c_int32]),
         "cfg_workspace_init": (c_int32, [vp, c_size_t, vp]),
+        "cfg_workspace_flush": (c_int32, [vp, c_size_t, vp]),
         "cfg_relmae_reduce": (c_int32, [vp, vp, c_int64, c_int32, vp, vp, POINTER(SchedParamsC),
                                         c_int32, vp, c_size_t, vp]),
         "cfg_ddim_step": (c_int32, [vp, vp, vp, vp, c_int64, c_int32, c_float, c_double, c_double,
@@ -148,12 +151,14 @@ class SchedParams:
     """tau1/tau2 rule parameters (L, k, g_slope, tau_cap, n_steps); see cfg_sched_params."""
 
     def __init__(self, n_steps: int, L: int = 5, g_slope: float = 1e-3, k: int = 10,
-                 tau_cap: int = -1):
-        self.c = SchedParamsC(L=L, k=k, g_slope=g_slope, tau_cap=tau_cap, n_steps=n_steps)
+                 tau_cap: int = -1, defer: bool = False):
+        self.c = SchedParamsC(L=L, k=k, g_slope=g_slope, tau_cap=tau_cap, n_steps=n_steps,
+                              flags=SCHED_DEFER if defer else 0, reserved=0)
 
     def __repr__(self) -> str:
         c = self.c
-        return f"SchedParams(n_steps={c.n_steps}, L={c.L}, g_slope={c.g_slope}, k={c.k}, tau_cap={c.tau_cap})"
+        return (f"SchedParams(n_steps={c.n_steps}, L={c.L}, g_slope={c.g_slope}, k={c.k}, "
+                f"tau_cap={c.tau_cap}, defer={bool(c.flags & SCHED_DEFER)})")
 
 
 def _sp(sched: Optional[SchedParams]):
@@ -177,6 +182,12 @@ def new_sched_state(device=None):
     """Device memory for one cfg_sched_state (contents are reset by step 0)."""
     torch = _torch()
     return torch.zeros(ctypes.sizeof(SchedStateC), dtype=torch.uint8, device=device or "cuda")
+
+
+def workspace_flush(workspace, stream=None) -> None:
+    """Complete a rel-MAE deferred in the workspace by a deferring step."""
+    ws, wsb = _ws(workspace)
+    _check(lib.cfg_workspace_flush(ws, wsb, _stream(stream)))
 
 
 def read_sched_state(state) -> Dict[str, object]:

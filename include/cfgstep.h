@@ -31,7 +31,8 @@
  *   - Latents are dense, contiguous arrays of `n` elements in any order the
  *     caller likes (the step is elementwise apart from the global sums), in
  *     fp32 (CFG_F32) or bf16 (CFG_BF16).  Arithmetic is fp32; the rel-MAE
- *     sums are combined in fp64.  16-byte aligned pointers take the 128-bit
+ *     sums are carried in double-fp32 (about 48 significant bits) and the
+ *     ratio is formed in fp64.  16-byte aligned pointers take the 128-bit
  *     vector path; any other alignment is accepted and takes a scalar path.
  *   - `x_out` may alias `x_in` (in-place update).
  *   - Return value: CFG_OK (0) or a negative cfg_status.  On error nothing
@@ -85,6 +86,12 @@ enum cfg_phase { CFG_PHASE_WARMUP = 0, CFG_PHASE_PARALLEL = 1, CFG_PHASE_FULL = 
 
 /* cfg_sched_state.flags bits. */
 #define CFG_SCHED_FLAG_OUT_OF_ORDER 1u /* a step index arrived that was not n_seen */
+#define CFG_SCHED_FLAG_DEFER_CLASH 2u  /* a deferred step was followed by a launch on the same
+                                          workspace writing the same partial slot (a step of the
+                                          same parity); its rel-MAE was dropped */
+
+/* cfg_sched_params.flags bits. */
+#define CFG_SCHED_DEFER 1u /* defer each step's rel-MAE to the next launch (see below) */
 
 /*
  * Parameters of the tau1/tau2 rule (Hybridiff notes, key design 3).  Host
@@ -95,7 +102,20 @@ enum cfg_phase { CFG_PHASE_WARMUP = 0, CFG_PHASE_PARALLEL = 1, CFG_PHASE_FULL = 
  *   tau_cap  >= 0: a calibrated safety cap (the step index of the minimum of
  *            a previously measured discrepancy curve); -1: the earliest
  *            argmin of this run's own rel-MAE trace, known after the last step;
- *   n_steps  steps in the run, 1..CFG_SCHED_MAX_STEPS.
+ *   n_steps  steps in the run, 1..CFG_SCHED_MAX_STEPS;
+ *   flags    0, or CFG_SCHED_DEFER: every step except the run's last leaves
+ *            the combine of its rel-MAE partial sums (and the schedule
+ *            update and M_out write of that step) to the next launch on the
+ *            same workspace, which does it in a side block while streaming
+ *            its own data -- the reduction's latency leaves the critical
+ *            path.  The next launch on that workspace must be the next
+ *            step (the other step parity), a call that finishes in-launch
+ *            (a non-deferred step, cfg_relmae_reduce), or cfg_workspace_flush;
+ *            a same-parity deferred step instead drops it and sets
+ *            CFG_SCHED_FLAG_DEFER_CLASH.  The last step of the run
+ *            (n_steps - 1) always finishes in-launch, so a finished run's
+ *            state is complete;
+ *   reserved must be 0.
  * The "t" of the notes' rule is read as the step index s, counted from the
  * first denoising step (s = 0 at the noisiest timestep).
  */
@@ -105,6 +125,8 @@ typedef struct cfg_sched_params {
   double g_slope;
   int32_t tau_cap;
   int32_t n_steps;
+  uint32_t flags;
+  int32_t reserved;
 } cfg_sched_params;
 
 /*
@@ -142,8 +164,8 @@ typedef struct cfg_sched_state {
 
 /*
  * Bytes of device workspace a step or reduction over `n` elements of
- * `dtype` needs (the per-block partial sums of the rel-MAE reduction and a
- * completion counter).  The value does not depend on the device.  Returns 0
+ * `dtype` needs (a header with a completion counter and the descriptor of a
+ * deferred reduction, then three slots of per-block partial sums).  The value does not depend on the device.  Returns 0
  * for an unsupported dtype or n < 0.
  */
 CFG_API size_t cfg_workspace_bytes(int64_t n, int32_t dtype);
@@ -156,6 +178,13 @@ CFG_API size_t cfg_workspace_bytes(int64_t n, int32_t dtype);
  * One workspace must not be used by two calls that may run concurrently.
  */
 CFG_API int cfg_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Complete a deferred rel-MAE left in the workspace by a step launched with
+ * CFG_SCHED_DEFER (writes its M_out and schedule update); a no-op when none
+ * is pending.  One single-block launch on `stream`.
+ */
+CFG_API int cfg_workspace_flush(void* ws, size_t ws_bytes, void* stream);
 
 /*
  * rel-MAE alone (Hybridiff notes, key design 2; with the velocity pair for

@@ -54,12 +54,14 @@ int main(void) {
   printf("cfg_sched_params %zu\n", sizeof(cfg_sched_params));
   printf("cfg_sched_state %zu\n", sizeof(cfg_sched_state));
   F(cfg_sched_params, L); F(cfg_sched_params, k); F(cfg_sched_params, g_slope);
-  F(cfg_sched_params, tau_cap); F(cfg_sched_params, n_steps);
+  F(cfg_sched_params, tau_cap); F(cfg_sched_params, n_steps); F(cfg_sched_params, flags);
+  F(cfg_sched_params, reserved);
   F(cfg_sched_state, n_seen); F(cfg_sched_state, tau1p); F(cfg_sched_state, argmin);
   F(cfg_sched_state, tau_cap); F(cfg_sched_state, tau1); F(cfg_sched_state, tau2);
   F(cfg_sched_state, decided_at); F(cfg_sched_state, flags); F(cfg_sched_state, min_M);
   F(cfg_sched_state, M); F(cfg_sched_state, G); F(cfg_sched_state, phase);
   printf("CFG_TAU_NONE %d\nCFG_SCHED_MAX_STEPS %d\n", CFG_TAU_NONE, CFG_SCHED_MAX_STEPS);
+  printf("CFG_SCHED_DEFER %u\nCFG_SCHED_FLAG_DEFER_CLASH %u\n", CFG_SCHED_DEFER, CFG_SCHED_FLAG_DEFER_CLASH);
   return 0;
 }
 ''')
@@ -77,6 +79,8 @@ int main(void) {
             assert c[f"{name}.{field}"] == getattr(typ, field).offset, (name, field)
     assert c["CFG_TAU_NONE"] == cs.TAU_NONE == O.TAU_NONE
     assert c["CFG_SCHED_MAX_STEPS"] == cs.SCHED_MAX_STEPS
+    assert c["CFG_SCHED_DEFER"] == cs.SCHED_DEFER
+    assert c["CFG_SCHED_FLAG_DEFER_CLASH"] == cs.SCHED_FLAG_DEFER_CLASH
 
 
 def test_version_and_workspace_size():
@@ -143,6 +147,12 @@ def test_schedule_arguments_validated():
         sp = cs.SchedParams(**p)
         assert _ddim(st=st, sp=ctypes.byref(sp.c), step=step) == -1
         assert cs.lib.cfg_sched_observe(st, ctypes.byref(sp.c), step, 0.5, None) == -1
+    bad = cs.SchedParams(n_steps=10)
+    bad.c.flags = 4
+    assert _ddim(st=st, sp=ctypes.byref(bad.c)) == -1          # unknown flag bit
+    bad = cs.SchedParams(n_steps=10)
+    bad.c.reserved = 1
+    assert _ddim(st=st, sp=ctypes.byref(bad.c)) == -1
     sp = cs.SchedParams(n_steps=10)
     # state without parameters (or the reverse) is rejected
     assert _ddim(st=st, sp=None) == -1
@@ -164,6 +174,8 @@ def test_other_entry_points_validate():
     assert L.cfg_randn(None, 0, 0, 0, 0, None) == 0          # empty request: nothing to do
     assert L.cfg_workspace_init(None, wsb, None) == -3
     assert L.cfg_workspace_init(FAKE, 8, None) == -3
+    assert L.cfg_workspace_flush(None, wsb, None) == -3
+    assert L.cfg_workspace_flush(FAKE, wsb - 16, None) == -3
     assert L.cfg_abar_linear(None, 10, 0.1, 0.2) == -1
     out = np.empty(4)
     assert L.cfg_abar_linear(out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), 4, 0.1, 1.5) == -1

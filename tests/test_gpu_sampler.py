@@ -4,8 +4,15 @@ Each workload is run end to end by the library's native sampler loop with the
 device-side synthetic denoiser, and by the oracle in float64 from the same
 stored x_T, means and perturbations.  Checked:
 
-* x_0: fp32 storage max abs error <= 1e-5; bf16 storage
-  max |g - o| / max(|o|, 1) <= 2e-2;
+* x_0: fp32 storage max abs error <= 1e-5; bf16 storage relative error
+  <= 2e-2 both norm-wise (||g - o||_2 / ||o||_2) and in the max norm
+  (max|g - o| / max|o|), and at most 1% of elements more than 1 bf16 ulp
+  apart.  Per element the free-running bf16 runs may differ by several ulps:
+  a 1-ulp difference in x late in the run changes the bf16 rounding of the
+  predictions, which the guidance scale w (and the 1/t of the flow
+  velocity) amplify.  This is a property of bf16 storage, reproduced
+  exactly by an fp32 emulation of the step on the CPU; the per-step check
+  (teacher forcing) holds every element to 1 ulp;
 * the rel-MAE trace: fp32 abs <= 1e-5 and rel <= 1e-6; bf16 rel <= 1e-3
   (the trajectories differ only by rare 1-ulp rounding disagreements);
 * tau1', tau_cap, tau1, tau2, decided_at and the phases: exactly equal to
@@ -20,7 +27,9 @@ import pytest
 import torch
 
 import workloads as W
-from gpu_harness import rel_err, run_workload
+import cfg_guided_sampler_step_b300 as cs
+from gpu_harness import (run_workload, to_device_stored, to_host_f64, ulp_distance_bf16,
+                         ulp_distance_f32)
 from oracle import cfg_oracle as O
 
 pytestmark = pytest.mark.gpu
@@ -42,7 +51,10 @@ def _check(wl, inputs, gpu, ref):
         assert float(np.max(np.abs(gpu.state["M"] - ref.M))) <= 1e-5
         assert float(np.max(np.abs(gpu.state["M"] / ref.M - 1))) <= 1e-6
     else:
-        assert rel_err(gpu.x0, ref.x0) <= 2e-2
+        d = gpu.x0 - ref.x0
+        assert np.linalg.norm(d) <= 2e-2 * np.linalg.norm(ref.x0)
+        assert np.max(np.abs(d)) <= 2e-2 * np.max(np.abs(ref.x0))
+        assert float(np.mean(ulp_distance_bf16(gpu.x0, ref.x0) > 1)) <= 0.01
         assert float(np.max(np.abs(gpu.state["M"] / ref.M - 1))) <= 1e-3
     st = gpu.state
     assert st["n_seen"] == wl.n_steps and st["flags"] == 0
@@ -75,6 +87,65 @@ def test_full_size_runs_match_oracle(cuda, name):
     gpu = run_workload(wl, inputs, cuda)
     ref = O.run_sampler(wl, inputs, perturb=_perturb(wl))
     _check(wl, inputs, gpu, ref)
+
+
+def _teacher_forced(wl, inputs, cuda):
+    """Every step of the oracle's run, replayed through the library on the oracle's own
+    stored x_s and predictions: each output element within 1 ulp of the oracle's x_{s+1}
+    (or, after cancellation to a tiny value, within 2^-17 for bf16 / 1e-9 for fp32),
+    each M_s within 1e-6 relative."""
+    pert = _perturb(wl)
+    ref = O.run_sampler(wl, inputs, perturb=pert, keep_trajectory=True)
+    reps = wl.n // inputs["mean_c"].size
+    mc = np.tile(inputs["mean_c"].reshape(-1).astype(np.float64), reps)
+    mu = np.tile(inputs["mean_u"].reshape(-1).astype(np.float64), reps)
+    ws = cs.new_workspace(wl.n, cs.CFG_F32 if wl.dtype == "f32" else cs.CFG_BF16, cuda)
+    M = torch.zeros(1, dtype=torch.float64, device=cuda)
+    N = wl.n_steps
+    if wl.mode == "ddim":
+        abar = O.abar_linear(wl.T, wl.beta_start, wl.beta_end)
+        ts = O.ddim_timesteps(N, wl.T)
+    else:
+        tg = O.flow_times(N)
+
+    def stored(v):
+        return O.f64_to_bf16_bits(v) if wl.dtype == "bf16" else v.astype(np.float32)
+
+    for s in range(N):
+        x = ref.trajectory[s]
+        if wl.mode == "ddim":
+            ab = float(abar[ts[s]])
+            abp = 1.0 if s == N - 1 else float(abar[ts[s + 1]])
+            c = O.gaussian_eps(x, mc, ab, wl.data_std, pert(s, "c") if pert else None, wl.dtype)
+            u = O.gaussian_eps(x, mu, ab, wl.data_std, pert(s, "u") if pert else None, wl.dtype)
+        else:
+            c = O.flow_velocity(x, mc, float(tg[s]), wl.dtype)
+            u = O.flow_velocity(x, mu, float(tg[s]), wl.dtype)
+        dx, dc, du = (to_device_stored(stored(v), wl.dtype, cuda) for v in (x, c, u))
+        out = torch.empty_like(dx)
+        if wl.mode == "ddim":
+            cs.ddim_step(out, dx, dc, du, w=wl.w, abar_t=ab, abar_prev=abp, eta=wl.eta,
+                         seed=wl.seed, step=s, M_out=M, workspace=ws)
+        else:
+            cs.flow_step(out, dx, dc, du, w=wl.w, t_cur=float(tg[s]), t_next=float(tg[s + 1]),
+                         step=s, M_out=M, workspace=ws)
+        torch.cuda.synchronize()
+        g = to_host_f64(out)
+        o = ref.trajectory[s + 1]
+        diff = np.abs(g - o)
+        if wl.dtype == "bf16":
+            ok = (ulp_distance_bf16(g, o) <= 1) | (diff <= 2.0**-17)
+        else:
+            assert float(diff.max()) <= 1e-5
+            ok = (ulp_distance_f32(g, o) <= 1) | (diff <= 1e-9)
+        assert ok.all(), (s, np.flatnonzero(~ok)[:5])
+        assert abs(M.item() / ref.M[s] - 1) <= 1e-6, s
+
+
+@pytest.mark.parametrize("name", W.WORKLOAD_ORDER)
+def test_full_size_teacher_forced_steps(cuda, name):
+    wl = W.WORKLOADS[name]
+    _teacher_forced(wl, W.draw_inputs(wl), cuda)
 
 
 def test_point_mass_run_lands_on_guided_mean(cuda):

@@ -288,3 +288,97 @@ def test_schedule_flags_out_of_order(cuda):
     assert got["flags"] & 1
     cs.sched_observe(st, sp, 0, 1.0)      # step 0 starts a new run
     assert cs.read_sched_state(st)["flags"] == 0
+
+
+# ---------------------------------------------------------------------------
+# Deferred reductions (CFG_SCHED_DEFER)
+# ---------------------------------------------------------------------------
+def _step_sequence(cuda, defer, n=200_003, N=12, dtype="bf16"):
+    """N consecutive DDIM steps on fixed random inputs; returns (x, per-step M, state)."""
+    code = _code(dtype)
+    preds = [_inputs(n, dtype, seed=400 + s, cuda=cuda) for s in range(N)]
+    abar = O.abar_linear()
+    ts = O.ddim_timesteps(N)
+    x = preds[0]["x"].clone()
+    Mbuf = torch.full((N,), -1.0, dtype=torch.float64, device=cuda)
+    st = cs.new_sched_state(cuda)
+    sp = cs.SchedParams(n_steps=N, L=2, g_slope=0.01, k=3, defer=defer)
+    ws = cs.new_workspace(n, code, cuda)
+    for s in range(N):
+        abp = 1.0 if s == N - 1 else float(abar[ts[s + 1]])
+        cs.ddim_step(x, x, preds[s]["c"], preds[s]["u"], w=4.0, abar_t=float(abar[ts[s]]),
+                     abar_prev=abp, eta=0.5, seed=9, step=s, M_out=Mbuf[s:s + 1], state=st,
+                     sched=sp, workspace=ws)
+    torch.cuda.synchronize()
+    return x.clone(), Mbuf.cpu().numpy(), cs.read_sched_state(st), preds
+
+
+def test_deferred_sequence_equals_synchronous(cuda):
+    xs, Ms, sts, preds = _step_sequence(cuda, defer=False)
+    xd, Md, std, _ = _step_sequence(cuda, defer=True)
+    assert torch.equal(xs, xd)
+    assert np.array_equal(Ms, Md) and np.all(Ms >= 0)
+    for key in ("n_seen", "tau1p", "argmin", "tau_cap", "tau1", "tau2", "decided_at", "flags"):
+        assert sts[key] == std[key], key
+    assert np.array_equal(sts["M"], std["M"]) and np.array_equal(sts["phase"], std["phase"])
+    # and the trace is the oracle's rel-MAE of each step's stored predictions
+    for s, p in enumerate(preds):
+        assert abs(Ms[s] / O.rel_mae(p["c64"], p["u64"]) - 1) <= 1e-6
+
+
+def test_deferred_step_completed_by_flush(cuda):
+    n = 70_001
+    d = _inputs(n, "bf16", seed=41, cuda=cuda)
+    ws = cs.new_workspace(n, cs.CFG_BF16, cuda)
+    st = cs.new_sched_state(cuda)
+    sp = cs.SchedParams(n_steps=10, defer=True)
+    M = torch.full((1,), -1.0, dtype=torch.float64, device=cuda)
+    out = torch.empty_like(d["x"])
+    ab, abp = float(O.abar_linear()[900]), float(O.abar_linear()[880])
+    cs.ddim_step(out, d["x"], d["c"], d["u"], w=3.0, abar_t=ab, abar_prev=abp, step=0, M_out=M,
+                 state=st, sched=sp, workspace=ws)
+    torch.cuda.synchronize()
+    assert M.item() == -1.0                      # deferred: not written yet
+    cs.workspace_flush(ws)
+    torch.cuda.synchronize()
+    assert abs(M.item() / O.rel_mae(d["c64"], d["u64"]) - 1) <= 1e-6
+    assert cs.read_sched_state(st)["n_seen"] == 1
+    cs.workspace_flush(ws)                       # nothing pending: a no-op
+    torch.cuda.synchronize()
+    assert cs.read_sched_state(st)["n_seen"] == 1
+
+
+def test_deferred_same_parity_clash_is_flagged(cuda):
+    n = 30_000
+    d = _inputs(n, "bf16", seed=43, cuda=cuda)
+    ws = cs.new_workspace(n, cs.CFG_BF16, cuda)
+    st = cs.new_sched_state(cuda)
+    sp = cs.SchedParams(n_steps=10, defer=True)
+    out = torch.empty_like(d["x"])
+    ab, abp = float(O.abar_linear()[900]), float(O.abar_linear()[880])
+    for step in (0, 2):                          # step 1 skipped: both write slot 0
+        cs.ddim_step(out, d["x"], d["c"], d["u"], w=3.0, abar_t=ab, abar_prev=abp, step=step,
+                     state=st, sched=sp, workspace=ws)
+    cs.workspace_flush(ws)
+    torch.cuda.synchronize()
+    got = cs.read_sched_state(st)
+    assert got["flags"] & cs.SCHED_FLAG_DEFER_CLASH
+    assert got["flags"] & cs.SCHED_FLAG_OUT_OF_ORDER     # step 2 recorded after step 0 was dropped
+
+
+def test_in_launch_call_completes_pending_step(cuda):
+    n = 40_000
+    d = _inputs(n, "f32", seed=47, cuda=cuda)
+    ws = cs.new_workspace(n, cs.CFG_F32, cuda)
+    st = cs.new_sched_state(cuda)
+    sp = cs.SchedParams(n_steps=5, defer=True)
+    M0 = torch.full((1,), -1.0, dtype=torch.float64, device=cuda)
+    M1 = torch.full((1,), -1.0, dtype=torch.float64, device=cuda)
+    out = torch.empty_like(d["x"])
+    ab, abp = float(O.abar_linear()[900]), float(O.abar_linear()[880])
+    cs.ddim_step(out, d["x"], d["c"], d["u"], w=3.0, abar_t=ab, abar_prev=abp, step=0, M_out=M0,
+                 state=st, sched=sp, workspace=ws)
+    cs.relmae_reduce(d["x"], d["u"], M_out=M1, workspace=ws)
+    torch.cuda.synchronize()
+    assert abs(M0.item() / O.rel_mae(d["c64"], d["u64"]) - 1) <= 1e-6
+    assert abs(M1.item() / O.rel_mae(d["x64"], d["u64"]) - 1) <= 1e-6
