@@ -81,6 +81,9 @@ def _load() -> ctypes.CDLL:
         "cfg_ddim_step": (c_int32, [vp, vp, vp, vp, c_int64, c_int32, c_float, c_double, c_double,
                                     c_float, c_uint64, c_int32, vp, vp, POINTER(SchedParamsC), vp,
                                     c_size_t, vp]),
+        "cfg_ddim_step_static_ws": (c_int32, [vp, vp, vp, vp, c_int64, c_int32, c_float, c_double,
+                                              c_double, c_float, c_uint64, c_int32, vp, vp,
+                                              POINTER(SchedParamsC), vp]),
         "cfg_flow_step": (c_int32, [vp, vp, vp, vp, c_int64, c_int32, c_float, c_double, c_double,
                                     c_int32, vp, vp, POINTER(SchedParamsC), vp, c_size_t, vp]),
         "cfg_sched_observe": (c_int32, [vp, POINTER(SchedParamsC), c_int32, c_double, vp]),
@@ -241,6 +244,19 @@ def ddim_step(x_out, x_in, pred_c, pred_u, *, w: float, abar_t: float, abar_prev
                              _dtype_code(x_out), w, abar_t, abar_prev, eta, seed, step,
                              _dev_ptr(M_out, "M_out"), _dev_ptr(state, "state"), _sp(sched), ws,
                              wsb, _stream(stream)))
+
+
+def ddim_step_static_ws(x_out, x_in, pred_c, pred_u, *, w: float, abar_t: float,
+                        abar_prev: float, eta: float = 0.0, seed: int = 0, step: int = 0,
+                        M_out=None, state=None, sched=None, stream=None) -> None:
+    """ddim_step on the library's static device scratch (no workspace argument), for callers
+    that cannot allocate device memory; calls on one device share that scratch."""
+    _same(x_out, x_in, pred_c, pred_u)
+    _check(lib.cfg_ddim_step_static_ws(
+        _dev_ptr(x_out, "x_out"), _dev_ptr(x_in, "x_in"), _dev_ptr(pred_c, "pred_c"),
+        _dev_ptr(pred_u, "pred_u"), x_out.numel(), _dtype_code(x_out), w, abar_t, abar_prev, eta,
+        seed, step, _dev_ptr(M_out, "M_out"), _dev_ptr(state, "state"), _sp(sched),
+        _stream(stream)))
 
 
 def flow_step(x_out, x_in, v_c, v_u, *, w: float, t_cur: float, t_next: float, workspace,

@@ -236,6 +236,37 @@ CFG_API int cfg_ddim_step(void* x_out, const void* x_in, const void* pred_c, con
                           size_t ws_bytes, void* stream);
 
 /*
+ * cfg_ddim_step without a caller-supplied workspace, for callers that cannot
+ * allocate device memory: code running where cudaMalloc is unavailable or
+ * forbidden (inside a host framework that owns every device allocation, a
+ * plugin or real-time path that must not allocate after start-up, an
+ * allocator-free embedding).  No counterpart on the source pages: it is a
+ * deployment convenience of this library, not part of the method.
+ *
+ * Arguments, results and errors are those of cfg_ddim_step, minus ws and
+ * ws_bytes.  The scratch is one static device array inside this library of
+ * cfg_workspace_bytes() = 196,864 bytes, held by every GPU that loads the
+ * library until the process exits.  It covers any n: the grid never exceeds
+ * the 4096 block partials the array holds; a request that would need more
+ * is rejected with CFG_ERR_WORKSPACE.  CFG_SCHED_DEFER is rejected
+ * (CFG_ERR_INVALID_ARG): every call finishes its rel-MAE in-launch.
+ *   - No allocation: the call uses no cudaMalloc, cudaFree or allocating
+ *     library routine.
+ *   - Set-up: the first call on each device (with that device current) looks
+ *     up the array's device address and zeroes its 256-byte header with a
+ *     synchronous cudaMemset; make that first call before any stream capture.
+ *   - Sharing: all calls on a device share the one array, which keeps the
+ *     last call's contents.  Calls that may overlap on the GPU (different
+ *     streams, or host threads without ordering) race on it: serialise them
+ *     on one stream.
+ */
+CFG_API int cfg_ddim_step_static_ws(void* x_out, const void* x_in, const void* pred_c,
+                                    const void* pred_u, int64_t n, int32_t dtype, float w,
+                                    double abar_t, double abar_prev, float eta, uint64_t seed,
+                                    int32_t step, double* M_out, cfg_sched_state* st,
+                                    const cfg_sched_params* sp, void* stream);
+
+/*
  * One fused CFG + Euler flow step (flow matching, Hybridiff notes "Loss /
  * training strategy": rel-MAE on the velocity pair):
  *   v     = v_u + w (v_c - v_u)
