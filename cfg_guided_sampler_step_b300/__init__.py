@@ -5,7 +5,7 @@ and the current CUDA stream to the C ABI declared in ``include/cfgstep.h``;
 all arithmetic of the step runs in the library's CUDA kernels.  PyTorch is
 used for device memory and streams.
 
-The library must be built (``python -m cfg_guided_sampler_step_b300._build``
+The library must be built (``python cfg_guided_sampler_step_b300/_build.py``
 or ``__graft_entry__.build()``); importing this package raises if it is
 missing -- there is no fallback path.
 """
@@ -66,7 +66,7 @@ DENOISE_FN = CFUNCTYPE(c_int32, c_void_p, c_int32, c_int32, c_double, c_void_p, 
 def _load() -> ctypes.CDLL:
     if not lib_path.exists():
         raise ImportError(
-            f"{lib_path} is not built; run `python -m cfg_guided_sampler_step_b300._build` "
+            f"{lib_path} is not built; run `python cfg_guided_sampler_step_b300/_build.py` "
             "(needs nvcc). There is no CPU fallback.")
     L = ctypes.CDLL(str(lib_path))
     vp = c_void_p

@@ -15,8 +15,13 @@ def pytest_configure(config):
 
 
 def _ensure_built():
-    from cfg_guided_sampler_step_b300 import _build
-    _build.build()
+    # loaded by path: importing the package needs the built library
+    import importlib.util
+    path = ROOT / "cfg_guided_sampler_step_b300" / "_build.py"
+    spec = importlib.util.spec_from_file_location("cfg_guided_sampler_step_b300_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
 
 
 # Build before any test module imports the binding (which raises when the
