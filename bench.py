@@ -227,8 +227,13 @@ def make_sets(wl, n_sets, device, torch):
     return sets
 
 
-def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clocks=None):
-    """Time exactly `steps` fused steps (plus `warmup` untimed) over rotating HBM-resident sets."""
+def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clocks=None,
+                sets=None):
+    """Time exactly `steps` fused steps (plus `warmup` untimed) over rotating HBM-resident sets.
+
+    `sets` overrides the number of buffer sets (default: >= 4x the L2 in whole sampler runs);
+    fewer sets keep a profiler capture small and are not used for timing.
+    """
     import torch
     import cfg_guided_sampler_step_b300 as cs
     props = torch.cuda.get_device_properties(device)
@@ -237,6 +242,8 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
     # enough sets for 4x the L2, rounded up to whole sampler runs
     n_sets = max(2, math.ceil(4 * l2 / set_bytes))
     n_sets = wl.n_steps * math.ceil(n_sets / wl.n_steps)
+    if sets:
+        n_sets = int(sets)
     sets = make_sets(wl, n_sets, device, torch)
     code = cs.CFG_F32 if wl.dtype == "f32" else cs.CFG_BF16
     ws = cs.new_workspace(wl.n, code, device)
@@ -308,8 +315,14 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
             "state_flags": state["flags"]}
 
 
-def time_e2e(wl: W.Workload, steps: int, device):
-    """Same metric through the public API with pinned host inputs and a host read of each result."""
+def time_e2e(wl: W.Workload, steps: int, device, depth: int = 3):
+    """Same metric through the public API with pinned host inputs and a host read of each result.
+
+    Every step copies its three inputs host->device, runs the step and copies its result and
+    M device->host, all inside the timed region.  As a serving loop would, consecutive steps
+    are pipelined over `depth` buffer slots on three streams (uploads, steps, downloads)
+    ordered by events, so one step's uploads overlap the previous step's download.
+    """
     import torch
     import cfg_guided_sampler_step_b300 as cs
     dt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
@@ -321,42 +334,62 @@ def time_e2e(wl: W.Workload, steps: int, device):
         return t.pin_memory()
 
     hx, hc, hu = host(inp["x"]), host(inp["c"]), host(inp["u"])
-    hout = torch.empty(wl.n, dtype=dt).pin_memory()
-    hM = torch.empty(1, dtype=torch.float64).pin_memory()
-    dx = torch.empty(wl.n, dtype=dt, device=device)
-    dc, du = torch.empty_like(dx), torch.empty_like(dx)
-    dM = torch.zeros(1, dtype=torch.float64, device=device)
+    slots = []
+    for _ in range(depth):
+        dx = torch.empty(wl.n, dtype=dt, device=device)
+        slots.append(dict(x=dx, c=torch.empty_like(dx), u=torch.empty_like(dx),
+                          M=torch.zeros(1, dtype=torch.float64, device=device),
+                          hout=torch.empty(wl.n, dtype=dt).pin_memory(),
+                          hM=torch.empty(1, dtype=torch.float64).pin_memory(),
+                          ev_in=torch.cuda.Event(), ev_run=torch.cuda.Event(),
+                          ev_out=torch.cuda.Event(), used=False))
     ws = cs.new_workspace(wl.n, cs.CFG_F32 if wl.dtype == "f32" else cs.CFG_BF16, device)
     st = cs.new_sched_state(device)
     # every step finishes its own reduction, so each step's M is complete when read back
     sp = cs.SchedParams(n_steps=wl.n_steps, L=wl.L, g_slope=wl.g_slope, k=wl.k, tau_cap=wl.tau_cap,
                         defer=False)
     plan = step_plan(wl, cs)
+    s_in, s_run, s_out = (torch.cuda.Stream(device) for _ in range(3))
 
     def one(i):
-        dx.copy_(hx, non_blocking=True)
-        dc.copy_(hc, non_blocking=True)
-        du.copy_(hu, non_blocking=True)
-        enqueue_step(cs, wl, (dx, dc, du), plan[i % wl.n_steps], ws, st, sp, M=dM)
-        hout.copy_(dx, non_blocking=True)
-        hM.copy_(dM, non_blocking=True)
+        sl = slots[i % depth]
+        with torch.cuda.stream(s_in):
+            if sl["used"]:
+                s_in.wait_event(sl["ev_out"])         # the slot's last result is on the host
+            sl["x"].copy_(hx, non_blocking=True)
+            sl["c"].copy_(hc, non_blocking=True)
+            sl["u"].copy_(hu, non_blocking=True)
+            sl["ev_in"].record(s_in)
+        with torch.cuda.stream(s_run):
+            s_run.wait_event(sl["ev_in"])
+            enqueue_step(cs, wl, (sl["x"], sl["c"], sl["u"]), plan[i % wl.n_steps], ws, st, sp,
+                         M=sl["M"])
+            sl["ev_run"].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(sl["ev_run"])
+            sl["hout"].copy_(sl["x"], non_blocking=True)
+            sl["hM"].copy_(sl["M"], non_blocking=True)
+            sl["ev_out"].record(s_out)
+        sl["used"] = True
 
-    for i in range(3):
+    for i in range(2 * depth):
         one(i)
     torch.cuda.synchronize(device)
-    stream = torch.cuda.current_stream(device)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
+    start.record(s_in)
+    s_run.wait_event(start)
+    s_out.wait_event(start)
     for i in range(steps):
         one(i)
-    end.record(stream)
+    end.record(s_out)
     end.synchronize()
+    torch.cuda.synchronize(device)
     ms = start.elapsed_time(end)
     eb = wl.elem_bytes
     return {"value": wl.n * steps / (ms * 1e-3), "unit": "latent elements/s",
             "h2d_bytes_per_step": 3 * wl.n * eb, "d2h_bytes_per_step": wl.n * eb + 8,
-            "steps": steps, "ms_per_step": ms / steps}
+            "steps": steps, "ms_per_step": ms / steps, "pipeline_depth": depth}
 
 
 # ---------------------------------------------------------------------------
@@ -433,6 +466,8 @@ def main(argv=None):
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--sets", type=int, default=None,
+                    help="buffer sets to rotate over (default: >= 4x L2); fewer only for profiling")
     args = ap.parse_args(argv)
     world, rank, local = dist_env()
     wl = W.WORKLOADS[args.workload]
@@ -476,7 +511,7 @@ def main(argv=None):
     clocks = ClockSampler(uuid) if rank == 0 else None
     if clocks:
         clocks.start()
-    dev = time_device(wl, args.steps, warmup, device, world, clocks)
+    dev = time_device(wl, args.steps, warmup, device, world, clocks, sets=args.sets)
     clk = clocks.stop() if clocks else None
     ms = max_over_ranks(dev["ms"], world, device)
     total_elems = sum_over_ranks(float(wl.n * args.steps), world, device)
@@ -494,8 +529,8 @@ def main(argv=None):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": dict(workload_config(wl), parallelism=f"replicas{world}",
                        l2=f"rotating {dev['n_sets']} buffer sets of {dev['set_bytes']} B "
-                          f"({dev['n_sets'] * dev['set_bytes'] / 2**20:.0f} MiB >= 4x the "
-                          f"{dev['l2_bytes'] / 2**20:.0f} MiB L2)",
+                          f"({dev['n_sets'] * dev['set_bytes'] / 2**20:.0f} MiB; the L2 holds "
+                          f"{dev['l2_bytes'] / 2**20:.0f} MiB)",
                        launch=f"CUDA graphs of {dev['graph_steps']} steps, programmatic dependent launch"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(wl.name),
@@ -504,7 +539,10 @@ def main(argv=None):
                      "algorithmic_bytes_per_launch": wl.bytes_per_step,
                      "frac_of_8tbs_spec": achieved / 8000.0},
         "e2e": {"value": e2e_v, "unit": e2e["unit"], "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
-                "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]},
+                "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+                "us_per_step": e2e["ms_per_step"] * 1e3,
+                "pipeline": f"{e2e['pipeline_depth']} buffer slots; upload, step and download "
+                            "streams ordered by events"},
         "gpu_launches": dev["launches"],
         "clocks": clk,
     }

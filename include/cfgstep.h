@@ -31,8 +31,11 @@
  *   - Latents are dense, contiguous arrays of `n` elements in any order the
  *     caller likes (the step is elementwise apart from the global sums), in
  *     fp32 (CFG_F32) or bf16 (CFG_BF16).  Arithmetic is fp32; the rel-MAE
- *     sums are carried in double-fp32 (about 48 significant bits) and the
- *     ratio is formed in fp64.  16-byte aligned pointers take the 128-bit
+ *     sums are carried in double-fp32 (about 48 significant bits) and their
+ *     ratio M is returned as an fp64 value within about 2^-44 of the
+ *     quotient of the two sums; the slope G = (M_s - M_{s-L}) / L is the
+ *     IEEE fp64 result (each operation correctly rounded).  Sums must stay
+ *     within the fp32 range.  16-byte aligned pointers take the 128-bit
  *     vector path; any other alignment is accepted and takes a scalar path.
  *   - `x_out` may alias `x_in` (in-place update).
  *   - Return value: CFG_OK (0) or a negative cfg_status.  On error nothing
@@ -104,17 +107,20 @@ enum cfg_phase { CFG_PHASE_WARMUP = 0, CFG_PHASE_PARALLEL = 1, CFG_PHASE_FULL = 
  *            argmin of this run's own rel-MAE trace, known after the last step;
  *   n_steps  steps in the run, 1..CFG_SCHED_MAX_STEPS;
  *   flags    0, or CFG_SCHED_DEFER: every step except the run's last leaves
- *            the combine of its rel-MAE partial sums (and the schedule
- *            update and M_out write of that step) to the next launch on the
- *            same workspace, which does it in a side block while streaming
- *            its own data -- the reduction's latency leaves the critical
- *            path.  The next launch on that workspace must be the next
- *            step (the other step parity), a call that finishes in-launch
- *            (a non-deferred step, cfg_relmae_reduce), or cfg_workspace_flush;
- *            a same-parity deferred step instead drops it and sets
- *            CFG_SCHED_FLAG_DEFER_CLASH.  The last step of the run
- *            (n_steps - 1) always finishes in-launch, so a finished run's
- *            state is complete;
+ *            the combine of its rel-MAE partial sums (and the M_out and M[s]
+ *            writes of that step) to the next launch on the same workspace,
+ *            and that launch leaves the step's schedule update to the launch
+ *            after it; each is done in a side block while those launches
+ *            stream their own data, so neither the reduction's latency nor
+ *            the rule's leaves a mark on the critical path.  The next launch
+ *            on that workspace must be the next step (the other step
+ *            parity), a call that finishes in-launch (a non-deferred step,
+ *            cfg_relmae_reduce), or cfg_workspace_flush; a same-parity
+ *            deferred step instead drops it and sets
+ *            CFG_SCHED_FLAG_DEFER_CLASH.  A launch that does not defer (the
+ *            last step of the run, n_steps - 1, always finishes in-launch)
+ *            completes all pending work first, so a finished run's state is
+ *            complete;
  *   reserved must be 0.
  * The "t" of the notes' rule is read as the step index s, counted from the
  * first denoising step (s = 0 at the noisiest timestep).
@@ -131,7 +137,7 @@ typedef struct cfg_sched_params {
 
 /*
  * Device-resident schedule state, one per sampler run (caller-allocated
- * device memory of sizeof(cfg_sched_state) bytes, 8-byte aligned; contents
+ * device memory of sizeof(cfg_sched_state) bytes, 16-byte aligned; contents
  * need no initialisation: step 0 resets it).  Updated by one device thread
  * after each step's rel-MAE is known; the host reads it whenever it likes.
  *   n_seen      steps recorded (the next expected step index);
@@ -180,9 +186,10 @@ CFG_API size_t cfg_workspace_bytes(int64_t n, int32_t dtype);
 CFG_API int cfg_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /*
- * Complete a deferred rel-MAE left in the workspace by a step launched with
- * CFG_SCHED_DEFER (writes its M_out and schedule update); a no-op when none
- * is pending.  One single-block launch on `stream`.
+ * Complete the work steps launched with CFG_SCHED_DEFER left in the
+ * workspace (a pending rel-MAE with its M_out write, and pending schedule
+ * updates); a no-op when none is pending.  One single-block launch on
+ * `stream`.
  */
 CFG_API int cfg_workspace_flush(void* ws, size_t ws_bytes, void* stream);
 

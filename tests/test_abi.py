@@ -158,6 +158,7 @@ def test_schedule_arguments_validated():
     assert _ddim(st=st, sp=None) == -1
     assert _ddim(st=None, sp=ctypes.byref(sp.c)) == -1
     assert _ddim(st=FAKE + 4, sp=ctypes.byref(sp.c)) == -1          # misaligned state
+    assert _ddim(st=FAKE + 8, sp=ctypes.byref(sp.c)) == -1          # state needs 16 bytes
 
 
 def test_other_entry_points_validate():
@@ -209,3 +210,25 @@ def test_sampler_run_validates_before_any_callback():
                                cb, None, FAKE, FAKE, ctypes.byref(sp5.c), FAKE, 0, FAKE,
                                cs.workspace_bytes(16, 1), None)
     assert r == -1 and not called
+
+
+def test_division_by_reciprocal_and_fma_is_correctly_rounded():
+    """The schedule's slope G = d / L is formed on the device as q0 = RN(d * y),
+    r = RN(d - q0 * L) (an FMA), G = RN(q0 + r * y) (an FMA) with y = RN(1/L);
+    Markstein's theorem says this is the correctly rounded quotient.  Checked here
+    with exact rational arithmetic (Fraction -> float rounds to nearest even) against
+    Python's correctly rounded float division, on random and adversarial d and L."""
+    from fractions import Fraction as F
+    g = np.random.default_rng(77)
+    Ls = [1, 2, 3, 5, 6, 7, 9, 10, 11, 13, 25, 97, 1000, 1023, 2**20 + 1, 2**31 - 1]
+    ds = list(g.standard_normal(3000) * 10.0 ** g.integers(-250, 250, 3000))
+    ds += [float(np.nextafter(1.0, 2.0)), 1.0 - 2.0**-53, 2.0**-890, 3.0 * 2.0**-880, 1e300]
+    for L in Ls:
+        y = F(1.0 / L)
+        for d in ds:
+            dF = F(d)
+            q0 = float(dF * y)
+            r = float(dF - F(q0) * L)
+            assert F(r) == dF - F(q0) * L          # the residual is exact
+            q = float(F(q0) + F(r) * y)
+            assert q == d / L, (d, L, q, d / L)

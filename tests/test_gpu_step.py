@@ -277,6 +277,50 @@ def test_schedule_random_traces_match_oracle(cuda):
         ref = O.schedule(M, L, gs, k, cap)
         assert {k_: got[k_] for k_ in ref.as_dict()} == ref.as_dict(), trial
         assert np.array_equal(got["phase"], ref.phase)
+        assert np.array_equal(got["G"], ref.G, equal_nan=True), trial
+
+
+def test_schedule_signed_zero_inf_nan_traces(cuda):
+    """The rule's comparisons on the device follow IEEE semantics exactly: negative M,
+    -0.0 against +0.0, infinities and NaN (which compares false), against the oracle."""
+    inf, nan = math.inf, math.nan
+    traces = [
+        [0.3, -0.0, 0.0, -0.0, 0.2, 0.2, -1.0, -1.0, 0.5, 0.5],
+        [1.0, 2.0, inf, inf, 3.0, -inf, 0.0, 0.0, 1e-300, 0.0],
+        [nan, 0.1, 0.1, nan, 0.1001, 0.1, -0.1, -0.1, 0.0, -0.0],
+        [5.0, 4.0, 3.0, 2.0, 1.0, 0.0, -1.0, -2.0, -3.0, -4.0],
+    ]
+    for L in (1, 2, 3):
+        for gs in (1e-3, 0.0, -0.0, 1.0, 5e-324):
+            for M in traces:
+                M = np.array(M, dtype=np.float64)
+                st = cs.new_sched_state(cuda)
+                sp = cs.SchedParams(n_steps=len(M), L=L, g_slope=gs, k=2)
+                for s_, m in enumerate(M):
+                    cs.sched_observe(st, sp, s_, float(m))
+                got = cs.read_sched_state(st)
+                ref = O.schedule(M, L, gs, 2, -1)
+                assert {k_: got[k_] for k_ in ref.as_dict()} == ref.as_dict(), (L, gs, M)
+                assert np.array_equal(got["G"], ref.G, equal_nan=True)
+                assert np.array_equal(got["phase"], ref.phase)
+
+
+@pytest.mark.parametrize("L", [1, 2, 3, 5, 7, 10, 11, 13, 97, 1000])
+def test_slope_is_ieee_division(cuda, L):
+    """G_s on the device equals fp64 (M_s - M_{s-L}) / L bit for bit, over traces of
+    widely varying magnitude (including exact repeats, i.e. zero differences)."""
+    g = np.random.default_rng(1000 + L)
+    N = 1024
+    M = np.abs(g.standard_normal(N)) * 10.0 ** g.integers(-30, 30, N)
+    M[L + 5] = M[5]                                  # a zero difference
+    st = cs.new_sched_state(cuda)
+    sp = cs.SchedParams(n_steps=N, L=L, g_slope=1e-3, k=3)
+    for s_ in range(N):
+        cs.sched_observe(st, sp, s_, float(M[s_]))
+    got = cs.read_sched_state(st)["G"]
+    ref = np.full(N, np.nan)
+    ref[L:] = (M[L:] - M[:-L]) / float(L)
+    assert np.array_equal(got, ref, equal_nan=True)
 
 
 def test_schedule_flags_out_of_order(cuda):
