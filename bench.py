@@ -202,16 +202,16 @@ def step_plan(wl: W.Workload, cs):
     return [dict(step=s, t_cur=1.0 - s / N, t_next=1.0 - (s + 1) / N) for s in range(N)]
 
 
-def enqueue_step(cs, wl, bufs, plan_s, ws, st, sp, M=None):
+def enqueue_step(cs, wl, bufs, plan_s, ws, st, sp, M=None, batch=1):
     x, pc, pu = bufs[:3]
     xo = bufs[3] if len(bufs) > 3 else x
     if wl.mode == "ddim":
         cs.ddim_step(xo, x, pc, pu, w=wl.w, abar_t=plan_s["abar_t"], abar_prev=plan_s["abar_prev"],
                      eta=wl.eta, seed=wl.seed, step=plan_s["step"], M_out=M, state=st, sched=sp,
-                     workspace=ws)
+                     workspace=ws, batch=batch)
     else:
         cs.flow_step(xo, x, pc, pu, w=wl.w, t_cur=plan_s["t_cur"], t_next=plan_s["t_next"],
-                     step=plan_s["step"], M_out=M, state=st, sched=sp, workspace=ws)
+                     step=plan_s["step"], M_out=M, state=st, sched=sp, workspace=ws, batch=batch)
 
 
 def make_sets(wl, n_sets, device, torch):
@@ -228,11 +228,12 @@ def make_sets(wl, n_sets, device, torch):
 
 
 def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clocks=None,
-                sets=None):
+                sets=None, batch=1):
     """Time exactly `steps` fused steps (plus `warmup` untimed) over rotating HBM-resident sets.
 
     `sets` overrides the number of buffer sets (default: >= 4x the L2 in whole sampler runs);
-    fewer sets keep a profiler capture small and are not used for timing.
+    fewer sets keep a profiler capture small and are not used for timing.  `batch` > 1 times
+    the batched step (a rel-MAE and schedule per sample).
     """
     import torch
     import cfg_guided_sampler_step_b300 as cs
@@ -246,8 +247,8 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
         n_sets = int(sets)
     sets = make_sets(wl, n_sets, device, torch)
     code = cs.CFG_F32 if wl.dtype == "f32" else cs.CFG_BF16
-    ws = cs.new_workspace(wl.n, code, device)
-    st = cs.new_sched_state(device)
+    ws = cs.new_workspace(wl.n, code, device, batch=batch)
+    st = cs.new_sched_state(device, batch=batch)
     # as in a sampler run: each step's reduction is completed by the next step's launch
     sp = cs.SchedParams(n_steps=wl.n_steps, L=wl.L, g_slope=wl.g_slope, k=wl.k, tau_cap=wl.tau_cap,
                         defer=True)
@@ -265,15 +266,17 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
         s.wait_stream(torch.cuda.current_stream(device))
         with torch.cuda.stream(s):
             for j in range(min(count, 8)):          # eager warm-up of the launch path
-                enqueue_step(cs, wl, sets[j % n_sets], plan[j % wl.n_steps], ws, st, sp)
-            cs.workspace_flush(ws)
+                enqueue_step(cs, wl, sets[j % n_sets], plan[j % wl.n_steps], ws, st, sp,
+                             batch=batch)
+            cs.workspace_flush(ws, batch=batch)
         torch.cuda.current_stream(device).wait_stream(s)
         torch.cuda.synchronize(device)
         with torch.cuda.graph(g, stream=s):
             for j in range(count):
-                enqueue_step(cs, wl, sets[j % n_sets], plan[j % wl.n_steps], ws, st, sp)
+                enqueue_step(cs, wl, sets[j % n_sets], plan[j % wl.n_steps], ws, st, sp,
+                             batch=batch)
             if count % wl.n_steps:
-                cs.workspace_flush(ws)
+                cs.workspace_flush(ws, batch=batch)
         torch.cuda.synchronize(device)
         return g
 
@@ -390,6 +393,84 @@ def time_e2e(wl: W.Workload, steps: int, device, depth: int = 3):
     return {"value": wl.n * steps / (ms * 1e-3), "unit": "latent elements/s",
             "h2d_bytes_per_step": 3 * wl.n * eb, "d2h_bytes_per_step": wl.n * eb + 8,
             "steps": steps, "ms_per_step": ms / steps, "pipeline_depth": depth}
+
+
+def time_sampler_runs(wl: W.Workload, device, runs: int = 20):
+    """Whole sampler runs of the workload through the public API, per denoising step.
+
+    Each step runs a synthetic Gaussian denoiser (fp32 torch ops, the model stand-in) for
+    both branches and the fused step: (1) ``sampler_run``'s host loop, (2) the same run
+    recorded into one CUDA graph and replayed, (3) ``sampler_run_branches`` with the two
+    branches on two streams joined by events.  Reported as microseconds per step.
+    """
+    import torch
+    import cfg_guided_sampler_step_b300 as cs
+    dt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
+    inp = W.draw_inputs(wl)
+    reps = wl.n // int(np.prod(wl.mean_shape))
+    mc = torch.from_numpy(np.tile(inp["mean_c"].reshape(-1), reps)).to(device)
+    mu = torch.from_numpy(np.tile(inp["mean_u"].reshape(-1), reps)).to(device)
+    x_T = torch.randn(wl.n, device=device).to(dt)
+    x = torch.empty_like(x_T)
+    pc, pu = torch.empty_like(x), torch.empty_like(x)
+    std2 = wl.data_std * wl.data_std
+
+    def branch(b, step, timestep, t):
+        mean, out = (mc, pc) if b == 0 else (mu, pu)
+        if wl.mode == "ddim":
+            A = math.sqrt(1.0 - t) / (t * std2 + 1.0 - t)
+            out.copy_((x.float() - math.sqrt(t) * mean) * A)
+        else:
+            out.copy_((x.float() - mean) * (1.0 / t))
+
+    def both(step, timestep, t):
+        branch(0, step, timestep, t)
+        branch(1, step, timestep, t)
+
+    code = cs.CFG_F32 if wl.dtype == "f32" else cs.CFG_BF16
+    ws, st = cs.new_workspace(wl.n, code, device), cs.new_sched_state(device)
+    sp = cs.SchedParams(n_steps=wl.n_steps, L=wl.L, g_slope=wl.g_slope, k=wl.k, tau_cap=wl.tau_cap)
+    kw = dict(mode=cs.CFG_MODE_DDIM if wl.mode == "ddim" else cs.CFG_MODE_FLOW,
+              n_steps=wl.n_steps, w=wl.w, pred_c=pc, pred_u=pu, sched=sp, state=st, workspace=ws,
+              eta=wl.eta, seed=wl.seed)
+    if wl.mode == "ddim":
+        kw["abar_table"] = cs.abar_linear(wl.T, wl.beta_start, wl.beta_end)
+        kw["timesteps"] = cs.ddim_timesteps(wl.n_steps, wl.T)
+    s = torch.cuda.Stream(device)
+    sc, su = torch.cuda.Stream(device), torch.cuda.Stream(device)
+
+    def eager():
+        x.copy_(x_T)
+        cs.sampler_run(x, denoise=both, **kw)
+
+    def branches():
+        x.copy_(x_T)
+        cs.sampler_run_branches(x, denoise_branch=branch, stream_c=sc, stream_u=su, **kw)
+
+    def timed(fn):
+        with torch.cuda.stream(s):
+            fn()
+            torch.cuda.synchronize(device)
+            t0 = time.perf_counter()
+            for _ in range(runs):
+                fn()
+            torch.cuda.synchronize(device)
+        return (time.perf_counter() - t0) / runs / wl.n_steps * 1e6
+
+    res = {"eager_us_per_step": timed(eager), "branch_streams_us_per_step": timed(branches)}
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        eager()
+    g.replay()
+    torch.cuda.synchronize(device)
+    t0 = time.perf_counter()
+    for _ in range(runs):
+        g.replay()
+    torch.cuda.synchronize(device)
+    res["graph_us_per_step"] = (time.perf_counter() - t0) / runs / wl.n_steps * 1e6
+    res["denoiser"] = "synthetic Gaussian posterior-mean denoiser, fp32 torch ops, both branches"
+    res["timer"] = "host wall clock around whole runs, device synchronised"
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -546,6 +627,8 @@ def main(argv=None):
         "gpu_launches": dev["launches"],
         "clocks": clk,
     }
+    if world == 1 and not args.no_sweep:
+        line["sampler_run"] = time_sampler_runs(wl, device)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     if world == 1 and not args.no_sweep:
@@ -560,6 +643,14 @@ def main(argv=None):
                            "achieved_gbs": w2.bytes_per_step / s / 1e9,
                            "frac": w2.bytes_per_step / s / 1e9 / peak,
                            "traffic": profiled_traffic(name)}
+        # the default workload again with a rel-MAE and tau1/tau2 schedule per sample
+        if wl.shape[0] > 1:
+            d2 = time_device(wl, args.sweep_steps, 2000, device, 1, batch=wl.shape[0])
+            s = d2["ms"] * 1e-3 / args.sweep_steps
+            sweep[f"{wl.name}/per_sample"] = {
+                "value": wl.n / s, "us_per_step": s * 1e6, "batch": wl.shape[0],
+                "achieved_gbs": wl.bytes_per_step / s / 1e9,
+                "frac": wl.bytes_per_step / s / 1e9 / peak}
         line["sweep"] = sweep
     print(json.dumps(line), flush=True)
     return 0

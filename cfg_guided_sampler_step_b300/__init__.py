@@ -24,7 +24,8 @@ __all__ = [
     "CFG_F32", "CFG_BF16", "CFG_MODE_DDIM", "CFG_MODE_FLOW", "TAU_NONE", "SCHED_MAX_STEPS",
     "CfgError", "SchedParams", "lib", "lib_path", "workspace_bytes", "new_workspace",
     "new_sched_state", "read_sched_state", "workspace_flush", "SCHED_DEFER", "relmae_reduce", "ddim_step", "flow_step",
-    "sched_observe", "randn", "abar_linear", "ddim_timesteps", "sampler_run", "version",
+    "sched_observe", "randn", "abar_linear", "ddim_timesteps", "abar_cosine", "timesteps",
+    "sampler_run", "sampler_run_branches", "version",
 ]
 
 CFG_F32, CFG_BF16 = 0, 1
@@ -56,11 +57,14 @@ class SchedStateC(Structure):
     _fields_ = [("n_seen", c_int32), ("tau1p", c_int32), ("argmin", c_int32), ("tau_cap", c_int32),
                 ("tau1", c_int32), ("tau2", c_int32), ("decided_at", c_int32), ("flags", c_uint32),
                 ("min_M", c_double), ("M", c_double * SCHED_MAX_STEPS),
-                ("G", c_double * SCHED_MAX_STEPS), ("phase", c_uint8 * SCHED_MAX_STEPS)]
+                ("G", c_double * SCHED_MAX_STEPS), ("phase", c_uint8 * SCHED_MAX_STEPS),
+                ("pad", c_uint8 * 8)]
 
 
 DENOISE_FN = CFUNCTYPE(c_int32, c_void_p, c_int32, c_int32, c_double, c_void_p, c_void_p, c_void_p,
                        c_void_p)
+BRANCH_FN = CFUNCTYPE(c_int32, c_void_p, c_int32, c_int32, c_int32, c_double, c_void_p, c_void_p,
+                      c_void_p)
 
 
 def _load() -> ctypes.CDLL:
@@ -86,10 +90,27 @@ def _load() -> ctypes.CDLL:
                                               POINTER(SchedParamsC), vp]),
         "cfg_flow_step": (c_int32, [vp, vp, vp, vp, c_int64, c_int32, c_float, c_double, c_double,
                                     c_int32, vp, vp, POINTER(SchedParamsC), vp, c_size_t, vp]),
+        "cfg_relmae_reduce_batched": (c_int32, [vp, vp, c_int64, c_int32, c_int32, vp, vp,
+                                                POINTER(SchedParamsC), c_int32, vp, c_size_t, vp]),
+        "cfg_ddim_step_batched": (c_int32, [vp, vp, vp, vp, c_int64, c_int32, c_int32, c_float,
+                                            c_double, c_double, c_float, c_uint64, c_int32, vp, vp,
+                                            POINTER(SchedParamsC), vp, c_size_t, vp]),
+        "cfg_flow_step_batched": (c_int32, [vp, vp, vp, vp, c_int64, c_int32, c_int32, c_float,
+                                            c_double, c_double, c_int32, vp, vp,
+                                            POINTER(SchedParamsC), vp, c_size_t, vp]),
+        "cfg_workspace_init_batched": (c_int32, [vp, c_size_t, c_int32, vp]),
+        "cfg_workspace_flush_batched": (c_int32, [vp, c_size_t, c_int32, vp]),
         "cfg_sched_observe": (c_int32, [vp, POINTER(SchedParamsC), c_int32, c_double, vp]),
+        "cfg_sampler_run_branches": (c_int32, [vp, c_int64, c_int32, c_int32, POINTER(c_double),
+                                               c_int32, POINTER(c_int32), POINTER(c_double),
+                                               c_int32, c_float, c_float, c_uint64, BRANCH_FN,
+                                               vp, vp, vp, vp, vp, POINTER(SchedParamsC), vp,
+                                               c_int32, vp, c_size_t, vp]),
         "cfg_randn": (c_int32, [vp, c_int64, c_uint64, c_uint32, c_uint32, vp]),
         "cfg_abar_linear": (c_int32, [POINTER(c_double), c_int32, c_double, c_double]),
         "cfg_ddim_timesteps": (c_int32, [POINTER(c_int32), c_int32, c_int32]),
+        "cfg_abar_cosine": (c_int32, [POINTER(c_double), c_int32, c_double, c_double]),
+        "cfg_timesteps": (c_int32, [POINTER(c_int32), c_int32, c_int32, c_int32]),
         "cfg_sampler_run": (c_int32, [vp, c_int64, c_int32, c_int32, POINTER(c_double), c_int32,
                                       POINTER(c_int32), POINTER(c_double), c_int32, c_float,
                                       c_float, c_uint64, DENOISE_FN, vp, vp, vp,
@@ -172,30 +193,33 @@ def workspace_bytes(n: int, dtype_code: int) -> int:
     return int(lib.cfg_workspace_bytes(n, dtype_code))
 
 
-def new_workspace(n: int = 0, dtype_code: int = CFG_BF16, device=None):
-    """A zero-filled (hence prepared) device workspace for calls over n elements."""
+def new_workspace(n: int = 0, dtype_code: int = CFG_BF16, device=None, batch: int = 1):
+    """A zero-filled (hence prepared) device workspace for calls over n elements
+    (``batch`` consecutive workspaces for the batched calls)."""
     torch = _torch()
     nb = workspace_bytes(n, dtype_code)
     if nb == 0:
         raise ValueError("invalid n / dtype for a workspace")
-    return torch.zeros(nb, dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(nb * batch, dtype=torch.uint8, device=device or "cuda")
 
 
-def new_sched_state(device=None):
-    """Device memory for one cfg_sched_state (contents are reset by step 0)."""
+def new_sched_state(device=None, batch: int = 1):
+    """Device memory for ``batch`` cfg_sched_state structs (contents are reset by step 0)."""
     torch = _torch()
-    return torch.zeros(ctypes.sizeof(SchedStateC), dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(ctypes.sizeof(SchedStateC) * batch, dtype=torch.uint8,
+                       device=device or "cuda")
 
 
-def workspace_flush(workspace, stream=None) -> None:
-    """Complete a rel-MAE deferred in the workspace by a deferring step."""
+def workspace_flush(workspace, stream=None, batch: int = 1) -> None:
+    """Complete the work deferring steps left in the workspace (``batch`` regions)."""
     ws, wsb = _ws(workspace)
-    _check(lib.cfg_workspace_flush(ws, wsb, _stream(stream)))
+    _check(lib.cfg_workspace_flush_batched(ws, wsb, batch, _stream(stream)))
 
 
-def read_sched_state(state) -> Dict[str, object]:
-    """Copy a device schedule state to the host (synchronises the current stream)."""
-    host = state.detach().to("cpu").numpy().tobytes()
+def read_sched_state(state, index: int = 0) -> Dict[str, object]:
+    """Copy schedule state ``index`` of a device state array to the host (synchronises)."""
+    size = ctypes.sizeof(SchedStateC)
+    host = state.detach().view(-1)[index * size:(index + 1) * size].to("cpu").numpy().tobytes()
     s = SchedStateC.from_buffer_copy(host)
     n = max(0, min(s.n_seen, SCHED_MAX_STEPS))
     return {
@@ -215,16 +239,23 @@ def _ws(workspace):
 # ---------------------------------------------------------------------------
 # Entry points
 # ---------------------------------------------------------------------------
+def _per_sample(t, batch: int) -> int:
+    if batch < 1 or t.numel() % batch:
+        raise ValueError(f"{t.numel()} elements do not split into {batch} samples")
+    return t.numel() // batch
+
+
 def relmae_reduce(pred_c, pred_u, *, workspace, M_out=None, state=None, sched=None, step: int = 0,
-                  stream=None) -> None:
-    """rel-MAE of (pred_c, pred_u) into M_out (float64 device scalar) and/or the schedule."""
+                  stream=None, batch: int = 1) -> None:
+    """rel-MAE of (pred_c, pred_u) into M_out (float64 device scalar, or ``batch`` of them,
+    one per sample) and/or the schedule state(s)."""
     if pred_c.shape != pred_u.shape or pred_c.dtype != pred_u.dtype:
         raise ValueError("pred_c and pred_u must match in shape and dtype")
     ws, wsb = _ws(workspace)
-    _check(lib.cfg_relmae_reduce(_dev_ptr(pred_c, "pred_c"), _dev_ptr(pred_u, "pred_u"),
-                                 pred_c.numel(), _dtype_code(pred_c), _dev_ptr(M_out, "M_out"),
-                                 _dev_ptr(state, "state"), _sp(sched), step, ws, wsb,
-                                 _stream(stream)))
+    _check(lib.cfg_relmae_reduce_batched(
+        _dev_ptr(pred_c, "pred_c"), _dev_ptr(pred_u, "pred_u"), _per_sample(pred_c, batch),
+        batch, _dtype_code(pred_c), _dev_ptr(M_out, "M_out"), _dev_ptr(state, "state"),
+        _sp(sched), step, ws, wsb, _stream(stream)))
 
 
 def _same(x_out, x_in, pc, pu) -> None:
@@ -235,15 +266,15 @@ def _same(x_out, x_in, pc, pu) -> None:
 
 def ddim_step(x_out, x_in, pred_c, pred_u, *, w: float, abar_t: float, abar_prev: float,
               workspace, eta: float = 0.0, seed: int = 0, step: int = 0, M_out=None, state=None,
-              sched=None, stream=None) -> None:
-    """One fused CFG + DDIM step (see cfg_ddim_step)."""
+              sched=None, stream=None, batch: int = 1) -> None:
+    """One fused CFG + DDIM step (see cfg_ddim_step; batch > 1: cfg_ddim_step_batched)."""
     _same(x_out, x_in, pred_c, pred_u)
     ws, wsb = _ws(workspace)
-    _check(lib.cfg_ddim_step(_dev_ptr(x_out, "x_out"), _dev_ptr(x_in, "x_in"),
-                             _dev_ptr(pred_c, "pred_c"), _dev_ptr(pred_u, "pred_u"), x_out.numel(),
-                             _dtype_code(x_out), w, abar_t, abar_prev, eta, seed, step,
-                             _dev_ptr(M_out, "M_out"), _dev_ptr(state, "state"), _sp(sched), ws,
-                             wsb, _stream(stream)))
+    _check(lib.cfg_ddim_step_batched(
+        _dev_ptr(x_out, "x_out"), _dev_ptr(x_in, "x_in"), _dev_ptr(pred_c, "pred_c"),
+        _dev_ptr(pred_u, "pred_u"), _per_sample(x_out, batch), batch, _dtype_code(x_out), w,
+        abar_t, abar_prev, eta, seed, step, _dev_ptr(M_out, "M_out"), _dev_ptr(state, "state"),
+        _sp(sched), ws, wsb, _stream(stream)))
 
 
 def ddim_step_static_ws(x_out, x_in, pred_c, pred_u, *, w: float, abar_t: float,
@@ -260,14 +291,16 @@ def ddim_step_static_ws(x_out, x_in, pred_c, pred_u, *, w: float, abar_t: float,
 
 
 def flow_step(x_out, x_in, v_c, v_u, *, w: float, t_cur: float, t_next: float, workspace,
-              step: int = 0, M_out=None, state=None, sched=None, stream=None) -> None:
-    """One fused CFG + Euler flow step (see cfg_flow_step)."""
+              step: int = 0, M_out=None, state=None, sched=None, stream=None,
+              batch: int = 1) -> None:
+    """One fused CFG + Euler flow step (see cfg_flow_step; batch > 1: cfg_flow_step_batched)."""
     _same(x_out, x_in, v_c, v_u)
     ws, wsb = _ws(workspace)
-    _check(lib.cfg_flow_step(_dev_ptr(x_out, "x_out"), _dev_ptr(x_in, "x_in"), _dev_ptr(v_c, "v_c"),
-                             _dev_ptr(v_u, "v_u"), x_out.numel(), _dtype_code(x_out), w, t_cur,
-                             t_next, step, _dev_ptr(M_out, "M_out"), _dev_ptr(state, "state"),
-                             _sp(sched), ws, wsb, _stream(stream)))
+    _check(lib.cfg_flow_step_batched(
+        _dev_ptr(x_out, "x_out"), _dev_ptr(x_in, "x_in"), _dev_ptr(v_c, "v_c"),
+        _dev_ptr(v_u, "v_u"), _per_sample(x_out, batch), batch, _dtype_code(x_out), w, t_cur,
+        t_next, step, _dev_ptr(M_out, "M_out"), _dev_ptr(state, "state"), _sp(sched), ws, wsb,
+        _stream(stream)))
 
 
 def sched_observe(state, sched: SchedParams, step: int, M: float, stream=None) -> None:
@@ -294,6 +327,23 @@ def ddim_timesteps(n_steps: int, T: int = 1000) -> np.ndarray:
     """DDIM timestep sequence, noisiest first (computed by the library)."""
     out = np.empty(n_steps, dtype=np.int32)
     _check(lib.cfg_ddim_timesteps(out.ctypes.data_as(POINTER(c_int32)), n_steps, T))
+    return out
+
+
+SPACING = {"linspace": 0, "leading": 1, "trailing": 2}
+
+
+def abar_cosine(T: int = 1000, s: float = 0.008, max_beta: float = 0.999) -> np.ndarray:
+    """Host table abar[t] of the cosine schedule (computed by the library)."""
+    out = np.empty(T, dtype=np.float64)
+    _check(lib.cfg_abar_cosine(out.ctypes.data_as(POINTER(c_double)), T, s, max_beta))
+    return out
+
+
+def timesteps(n_steps: int, T: int = 1000, spacing: str = "linspace") -> np.ndarray:
+    """Timestep sequence, noisiest first, with the given spacing (computed by the library)."""
+    out = np.empty(n_steps, dtype=np.int32)
+    _check(lib.cfg_timesteps(out.ctypes.data_as(POINTER(c_int32)), n_steps, T, SPACING[spacing]))
     return out
 
 
@@ -337,6 +387,56 @@ def sampler_run(x, *, mode: int, n_steps: int, w: float, denoise: Callable, pred
         0 if abar_table is None else int(abar_table.shape[0]), ts, tg, n_steps, w, eta, seed, cb,
         None, _dev_ptr(pred_c, "pred_c"), _dev_ptr(pred_u, "pred_u"), _sp(sched),
         _dev_ptr(state, "state"), start_step, ws, wsb, _stream(stream))
+    if err:
+        raise err[0]
+    _check(status)
+
+
+def sampler_run_branches(x, *, mode: int, n_steps: int, w: float, denoise_branch: Callable,
+                         pred_c, pred_u, stream_c, stream_u, sched: SchedParams, state,
+                         workspace, abar_table: Optional[np.ndarray] = None,
+                         timesteps: Optional[np.ndarray] = None,
+                         t_grid: Optional[np.ndarray] = None, eta: float = 0.0, seed: int = 0,
+                         start_step: int = 0, stream=None) -> None:
+    """A whole CFG sampler run with the two branches on two streams (see
+    cfg_sampler_run_branches).
+
+    ``denoise_branch(branch, step, timestep, t)`` must enqueue branch 0 (conditional, into
+    ``pred_c``) or 1 (unconditional, into ``pred_u``); it is called with that branch's stream
+    (``stream_c`` / ``stream_u``) as torch's current stream.
+    """
+    torch = _torch()
+    _same(x, x, pred_c, pred_u)
+    err = []
+    streams = {0: stream_c, 1: stream_u}
+
+    def _cb(user, branch, step, timestep, t, x_t, out, strm):
+        try:
+            with torch.cuda.stream(streams[int(branch)]):
+                denoise_branch(int(branch), int(step), int(timestep), float(t))
+            return 0
+        except BaseException as e:  # noqa: BLE001 - re-raised after the C loop returns
+            err.append(e)
+            return 1
+
+    cb = BRANCH_FN(_cb)
+    ab = ts = tg = None
+    if abar_table is not None:
+        abar_table = np.ascontiguousarray(abar_table, dtype=np.float64)
+        ab = abar_table.ctypes.data_as(POINTER(c_double))
+    if timesteps is not None:
+        timesteps = np.ascontiguousarray(timesteps, dtype=np.int32)
+        ts = timesteps.ctypes.data_as(POINTER(c_int32))
+    if t_grid is not None:
+        t_grid = np.ascontiguousarray(t_grid, dtype=np.float64)
+        tg = t_grid.ctypes.data_as(POINTER(c_double))
+    ws, wsb = _ws(workspace)
+    status = lib.cfg_sampler_run_branches(
+        _dev_ptr(x, "x"), x.numel(), _dtype_code(x), mode, ab,
+        0 if abar_table is None else int(abar_table.shape[0]), ts, tg, n_steps, w, eta, seed, cb,
+        None, _dev_ptr(pred_c, "pred_c"), _dev_ptr(pred_u, "pred_u"), _stream(stream_c),
+        _stream(stream_u), _sp(sched), _dev_ptr(state, "state"), start_step, ws, wsb,
+        _stream(stream))
     if err:
         raise err[0]
     _check(status)

@@ -1,7 +1,8 @@
 """Build step of the CUDA library: one nvcc invocation, in-tree.
 
-Produces ``libcfgstep.so`` next to this file from ``csrc/cfgstep.cu`` for
-sm_103a (B300).  Only the ``extern "C"`` entry points declared in
+Produces ``libcfgstep.so`` next to this file from ``csrc/cfgstep.cu`` (the
+kernels and the step entry points) and ``csrc/cfgstep_host.cpp`` (host tables
+and sampler loops) for sm_103a (B300).  Only the ``extern "C"`` entry points declared in
 ``include/cfgstep.h`` are exported (hidden visibility for everything else).
 """
 from __future__ import annotations
@@ -15,6 +16,8 @@ from pathlib import Path
 PKG_DIR = Path(__file__).resolve().parent
 REPO_DIR = PKG_DIR.parent
 SRC = PKG_DIR / "csrc" / "cfgstep.cu"
+SOURCES = [SRC, PKG_DIR / "csrc" / "cfgstep_host.cpp"]
+INTERNAL = PKG_DIR / "csrc" / "cfgstep_internal.h"
 HEADER = REPO_DIR / "include" / "cfgstep.h"
 LIB = PKG_DIR / "libcfgstep.so"
 
@@ -36,7 +39,7 @@ def nvcc_command(out: Path = LIB, extra: list[str] | None = None) -> list[str]:
         "-cudart", "shared", f"-Xlinker=-rpath,{cuda_lib}",
         "-I", str(HEADER.parent),
         *(extra or []),
-        "-o", str(out), str(SRC),
+        "-o", str(out), *map(str, SOURCES),
     ]
 
 
@@ -44,7 +47,7 @@ def needs_build() -> bool:
     if not LIB.exists():
         return True
     t = LIB.stat().st_mtime
-    return any(p.stat().st_mtime > t for p in (SRC, HEADER, Path(__file__)))
+    return any(p.stat().st_mtime > t for p in (*SOURCES, INTERNAL, HEADER, Path(__file__)))
 
 
 def build(force: bool = False, verbose: bool = False) -> Path:

@@ -166,6 +166,7 @@ typedef struct cfg_sched_state {
   double M[CFG_SCHED_MAX_STEPS];
   double G[CFG_SCHED_MAX_STEPS];
   uint8_t phase[CFG_SCHED_MAX_STEPS];
+  uint8_t pad[8]; /* sizeof is a multiple of 16, so arrays of states stay 16-byte aligned */
 } cfg_sched_state;
 
 /*
@@ -288,6 +289,51 @@ CFG_API int cfg_flow_step(void* x_out, const void* x_in, const void* v_c, const 
                           const cfg_sched_params* sp, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Batched forms: one launch over `batch` samples laid out back to back in
+ * every array (sample b is elements [b n, (b+1) n) with n = n_per_sample),
+ * each with its OWN rel-MAE and tau1/tau2 schedule -- the batch-level
+ * scale-out of the Hybridiff notes ("Loss / training strategy": every two
+ * GPUs produce one image, so each image has its own pair of branches and its
+ * own phases).  The update of every element is the unbatched step's (the
+ * eta noise counter is the element's index in the whole batch, so a batched
+ * step writes the same x as cfg_ddim_step over all batch * n elements); only
+ * the reduction and the schedule are per sample.
+ *   batch              1 .. 65535;
+ *   M_out              device, nullable: batch doubles (M_out[b]);
+ *   st                 device, nullable: batch consecutive cfg_sched_state
+ *                      structs (st[b]); sp (host) applies to every sample;
+ *   ws, ws_bytes       batch consecutive workspaces of cfg_workspace_bytes()
+ *                      bytes each (ws_bytes >= batch * cfg_workspace_bytes),
+ *                      prepared by cfg_workspace_init_batched (or zeroed);
+ *   CFG_SCHED_DEFER    works per sample as for the unbatched calls; complete
+ *                      pending work with cfg_workspace_flush_batched.
+ * The 128-bit vector path additionally needs n_per_sample * element size to
+ * be a multiple of 16 bytes; otherwise the call takes the scalar path.
+ * Arguments and errors are otherwise those of the unbatched calls.
+ */
+CFG_API int cfg_relmae_reduce_batched(const void* pred_c, const void* pred_u,
+                                      int64_t n_per_sample, int32_t batch, int32_t dtype,
+                                      double* M_out, cfg_sched_state* st,
+                                      const cfg_sched_params* sp, int32_t step, void* ws,
+                                      size_t ws_bytes, void* stream);
+CFG_API int cfg_ddim_step_batched(void* x_out, const void* x_in, const void* pred_c,
+                                  const void* pred_u, int64_t n_per_sample, int32_t batch,
+                                  int32_t dtype, float w, double abar_t, double abar_prev,
+                                  float eta, uint64_t seed, int32_t step, double* M_out,
+                                  cfg_sched_state* st, const cfg_sched_params* sp, void* ws,
+                                  size_t ws_bytes, void* stream);
+CFG_API int cfg_flow_step_batched(void* x_out, const void* x_in, const void* v_c,
+                                  const void* v_u, int64_t n_per_sample, int32_t batch,
+                                  int32_t dtype, float w, double t_cur, double t_next,
+                                  int32_t step, double* M_out, cfg_sched_state* st,
+                                  const cfg_sched_params* sp, void* ws, size_t ws_bytes,
+                                  void* stream);
+/* Prepare / flush `batch` consecutive workspaces (see cfg_workspace_init,
+ * cfg_workspace_flush); ws_bytes >= batch * cfg_workspace_bytes(...). */
+CFG_API int cfg_workspace_init_batched(void* ws, size_t ws_bytes, int32_t batch, void* stream);
+CFG_API int cfg_workspace_flush_batched(void* ws, size_t ws_bytes, int32_t batch, void* stream);
+
+/*
  * Record an externally computed rel-MAE value M as step `step` of the
  * schedule (for callers that reduce the discrepancy elsewhere, e.g. from
  * partial sums of a latent split across devices).  Enqueues one tiny
@@ -334,6 +380,37 @@ CFG_API int cfg_sampler_run(void* x, int64_t n, int32_t dtype, int32_t mode,
                             int32_t start_step, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Branch callback of cfg_sampler_run_branches: must enqueue on `stream` the
+ * prediction of one branch for x_t into `pred` (n elements of the run's
+ * dtype) -- branch 0: conditional, 1: unconditional -- and return 0, or
+ * return non-zero to stop the run.  `timestep` and `t` as cfg_denoise_fn.
+ */
+typedef int32_t (*cfg_branch_fn)(void* user, int32_t branch, int32_t step, int32_t timestep,
+                                 double t, const void* x_t, void* pred, void* stream);
+
+/*
+ * cfg_sampler_run in the CFG-parallel form of the xDiT review (section 3,
+ * "CFG Parallelism"): the conditional and the unconditional predictions are
+ * produced separately -- there on two GPUs and gathered before the
+ * scheduler, here on two streams of one GPU (`stream_c`, `stream_u`) and
+ * joined by events before each step on `stream`, so the two branches'
+ * kernels may run concurrently.  Every step: the branch streams wait for x_t
+ * on `stream`, the callback enqueues branch 0 on stream_c and branch 1 on
+ * stream_u, and `stream` waits for both before the fused step.  The three
+ * streams must differ.  Three events are created and destroyed inside the
+ * call (no device memory is allocated).  Arguments, results and errors are
+ * otherwise those of cfg_sampler_run.
+ */
+CFG_API int cfg_sampler_run_branches(void* x, int64_t n, int32_t dtype, int32_t mode,
+                                     const double* abar_table, int32_t T, const int32_t* timesteps,
+                                     const double* t_grid, int32_t n_steps, float w, float eta,
+                                     uint64_t seed, cfg_branch_fn fn, void* user,
+                                     void* pred_c_buf, void* pred_u_buf, void* stream_c,
+                                     void* stream_u, const cfg_sched_params* sp,
+                                     cfg_sched_state* st, int32_t start_step, void* ws,
+                                     size_t ws_bytes, void* stream);
+
+/*
  * Standard normal noise, the same stream the DDIM step draws for eta > 0:
  * out[i] = Box-Muller normal of element i from Philox4x32-10 with key
  * (seed low word, seed high word) and counter (i/4 low, i/4 high, step,
@@ -356,6 +433,29 @@ CFG_API int cfg_randn(float* out, int64_t n, uint64_t seed, uint32_t step, uint3
  */
 CFG_API int cfg_abar_linear(double* abar_out, int32_t T, double beta_start, double beta_end);
 CFG_API int cfg_ddim_timesteps(int32_t* out, int32_t n_steps, int32_t T);
+
+/*
+ * Adjacent samplers (host helpers, no device work).  The zyxy.net page names
+ * the "linear" and "cosine" noise schedules (section 1) and fewer, spaced
+ * sampling steps (section 3); these tables feed cfg_sampler_run and the
+ * step calls unchanged.
+ * cfg_abar_cosine: the cosine schedule of Nichol and Dhariwal ("Improved
+ *   denoising diffusion probabilistic models", 2021):
+ *   f(t) = cos^2(((t / T) + s) / (1 + s) * pi / 2),
+ *   beta_i = min(1 - f(i + 1) / f(i), max_beta),
+ *   abar[i] = prod_{j<=i} (1 - beta_j), sequential fp64 product.
+ *   abar_out: host, T doubles; T >= 1; s >= 0 finite (0.008 in the paper);
+ *   0 < max_beta < 1 (0.999 in the paper).
+ * cfg_timesteps: n_steps training timesteps, noisiest first, by `spacing`:
+ *   CFG_SPACING_LINSPACE  round(linspace(0, T-1, n_steps)) (cfg_ddim_timesteps);
+ *   CFG_SPACING_LEADING   i * (T / n_steps) (integer ratio), i = n_steps-1 .. 0;
+ *   CFG_SPACING_TRAILING  round(T - i * T / n_steps) - 1, i = 0 .. n_steps-1
+ *                         (ties to even), so the first step is T - 1.
+ *   out: host, n_steps int32; 1 <= n_steps <= T.
+ */
+enum cfg_spacing { CFG_SPACING_LINSPACE = 0, CFG_SPACING_LEADING = 1, CFG_SPACING_TRAILING = 2 };
+CFG_API int cfg_abar_cosine(double* abar_out, int32_t T, double s, double max_beta);
+CFG_API int cfg_timesteps(int32_t* out, int32_t n_steps, int32_t T, int32_t spacing);
 
 /* Message of the last failed call on this host thread ("" if none). */
 CFG_API const char* cfg_last_error(void);

@@ -147,6 +147,36 @@ def ddim_timesteps(N: int, T: int = 1000) -> np.ndarray:
     return seq[::-1].copy()
 
 
+def abar_cosine(T: int = 1000, s: float = 0.008, max_beta: float = 0.999) -> np.ndarray:
+    """[ZYX] section 1 names a cosine schedule; its definition (reading) is Nichol and
+    Dhariwal's: abar(t) = f(t)/f(0) with f(t) = cos^2(((t/T) + s)/(1 + s) * pi/2), applied
+    through beta_i = 1 - f(i+1)/f(i) clipped at max_beta, abar_i = prod_{j<=i} (1 - beta_j)
+    (sequential fp64 product)."""
+    def f(t):
+        return math.cos((t / T + s) / (1.0 + s) * math.pi / 2.0) ** 2
+    abar = np.empty(T, dtype=np.float64)
+    acc = 1.0
+    for i in range(T):
+        beta = min(1.0 - f(i + 1) / f(i), max_beta)
+        acc = acc * (1.0 - beta)
+        abar[i] = acc
+    return abar
+
+
+def timesteps(N: int, T: int = 1000, spacing: str = "linspace") -> np.ndarray:
+    """N training timesteps, noisiest first.  "linspace" is the [ZYX] DDIM rule; "leading"
+    (i * (T // N)) and "trailing" (round(T - i T/N) - 1, which starts at T - 1) are the
+    spacings of Lin et al. 2023 ("Common diffusion noise schedules and sample steps are
+    flawed") for fewer, spaced steps ([ZYX] section 3)."""
+    if spacing == "linspace":
+        return ddim_timesteps(N, T)
+    if spacing == "leading":
+        return (np.arange(N, dtype=np.int64) * (T // N))[::-1].copy()
+    if spacing == "trailing":
+        return np.array([int(np.round(T - i * (T / N))) - 1 for i in range(N)], dtype=np.int64)
+    raise ValueError(spacing)
+
+
 def flow_times(N: int) -> np.ndarray:
     """Uniform Euler grid on t in [1, 0]: t_i = 1 - i/N, i = 0..N (reading)."""
     return np.array([1.0 - i / N for i in range(N + 1)], dtype=np.float64)
@@ -170,6 +200,15 @@ def rel_mae(pred_c: np.ndarray, pred_u: np.ndarray) -> float:
             return math.nan
         return 0.0 if s_diff == 0.0 else math.inf
     return s_diff / s_u
+
+
+def rel_mae_per_sample(pred_c: np.ndarray, pred_u: np.ndarray, batch: int) -> np.ndarray:
+    """[HYB] loss/training strategy, batch-level scale-out: every image is produced by its own
+    pair of branches, so each of the ``batch`` samples (equal consecutive slices of the latent)
+    has its own discrepancy M_b = rel_mae(sample b's predictions)."""
+    c = np.asarray(pred_c, dtype=np.float64).reshape(batch, -1)
+    u = np.asarray(pred_u, dtype=np.float64).reshape(batch, -1)
+    return np.array([rel_mae(c[b], u[b]) for b in range(batch)], dtype=np.float64)
 
 
 def guidance(pred_c: np.ndarray, pred_u: np.ndarray, w: float) -> np.ndarray:
@@ -416,16 +455,20 @@ class RunResult:
     M: np.ndarray                  # rel-MAE trace [N]
     sched: Schedule
     trajectory: Optional[List[np.ndarray]] = None
+    M_samples: Optional[np.ndarray] = None          # [N, batch] per-sample traces
+    sched_samples: Optional[List[Schedule]] = None  # one schedule per sample
 
 
 def run_sampler(wl, inputs: Dict[str, np.ndarray], perturb: Optional[Callable] = None,
                 dtype: Optional[str] = None, keep_trajectory: bool = False,
-                w: Optional[float] = None) -> RunResult:
+                w: Optional[float] = None, batch: Optional[int] = None) -> RunResult:
     """The full N-step CFG sampler on a workload (``workloads.Workload``) in float64.
 
     ``inputs`` comes from ``workloads.draw_inputs``; ``perturb(step, branch)``
     supplies the per-step prediction perturbation (``workloads.draw_perturbation``).
-    ``dtype`` overrides the storage type ("f64" turns rounding off).
+    ``dtype`` overrides the storage type ("f64" turns rounding off).  With ``batch``,
+    the per-sample traces M_b and schedules of the batch-level scale-out are recorded too
+    (the update of x is the same).
     """
     dt = dtype or wl.dtype
     wv = wl.w if w is None else w
@@ -439,10 +482,12 @@ def run_sampler(wl, inputs: Dict[str, np.ndarray], perturb: Optional[Callable] =
     mu = np.tile(mu.reshape(-1), reps)
     N = wl.n_steps
     M = np.empty(N, dtype=np.float64)
+    MB = np.empty((N, batch), dtype=np.float64) if batch else None
     traj = [x.copy()] if keep_trajectory else None
     if wl.mode == "ddim":
-        abar = abar_linear(wl.T, wl.beta_start, wl.beta_end)
-        ts = ddim_timesteps(N, wl.T)
+        abar = (abar_cosine(wl.T) if wl.schedule == "cosine"
+                else abar_linear(wl.T, wl.beta_start, wl.beta_end))
+        ts = timesteps(N, wl.T, wl.spacing)
         for s in range(N):
             ab = float(abar[ts[s]])
             last = s == N - 1
@@ -451,6 +496,8 @@ def run_sampler(wl, inputs: Dict[str, np.ndarray], perturb: Optional[Callable] =
             pu = perturb(s, "u") if perturb else None
             c = gaussian_eps(x, mc, ab, wl.data_std, pc, dt)
             u = gaussian_eps(x, mu, ab, wl.data_std, pu, dt)
+            if batch:
+                MB[s] = rel_mae_per_sample(c, u, batch)
             x, M[s] = ddim_step(x, c, u, dt, wv, ab, ab_prev, wl.eta, wl.seed, s, last=last)
             if keep_trajectory:
                 traj.append(x.copy())
@@ -459,10 +506,14 @@ def run_sampler(wl, inputs: Dict[str, np.ndarray], perturb: Optional[Callable] =
         for s in range(N):
             c = flow_velocity(x, mc, float(t[s]), dt)
             u = flow_velocity(x, mu, float(t[s]), dt)
+            if batch:
+                MB[s] = rel_mae_per_sample(c, u, batch)
             x, M[s] = flow_step(x, c, u, dt, wv, float(t[s]), float(t[s + 1]))
             if keep_trajectory:
                 traj.append(x.copy())
     else:
         raise ValueError(wl.mode)
     sched = schedule(M, wl.L, wl.g_slope, wl.k, wl.tau_cap)
-    return RunResult(x, M, sched, traj)
+    sched_b = ([schedule(MB[:, b], wl.L, wl.g_slope, wl.k, wl.tau_cap) for b in range(batch)]
+               if batch else None)
+    return RunResult(x, M, sched, traj, MB, sched_b)

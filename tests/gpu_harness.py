@@ -58,6 +58,28 @@ class Denoiser:
             return None
         return torch.from_numpy(p.astype(np.float64)).to(self.x.device)
 
+    def branch(self, b: int, step: int, timestep: int, t: float) -> None:
+        """One branch only (0: conditional into pred_c, 1: unconditional into pred_u), with the
+        same arithmetic as __call__, on the current stream."""
+        self.calls += 1
+        wl = self.wl
+        mean, out, br = (self.mc, self.pc, "c") if b == 0 else (self.mu, self.pu, "u")
+        x64 = self.x.view(-1).to(torch.float64)
+        if wl.mode == "ddim":
+            abar = t
+            sa = math.sqrt(abar)
+            A = math.sqrt(1.0 - abar) / (abar * wl.data_std * wl.data_std + (1.0 - abar))
+            v = mean * sa
+            v = x64 - v
+            v = v * A
+            p = self._perturb(step, br)
+            if p is not None:
+                v = v + p
+        else:
+            v = x64 - mean
+            v = v * (1.0 / t)
+        self._store(v, out)
+
     def __call__(self, step: int, timestep: int, t: float) -> None:
         self.calls += 1
         wl = self.wl
@@ -107,8 +129,9 @@ def run_workload(wl: W.Workload, inputs: Dict[str, np.ndarray], device="cuda",
               n_steps=wl.n_steps, w=wl.w, denoise=den, pred_c=pc, pred_u=pu, sched=sp, state=st,
               workspace=ws, eta=wl.eta, seed=wl.seed, start_step=start)
     if wl.mode == "ddim":
-        kw["abar_table"] = cs.abar_linear(wl.T, wl.beta_start, wl.beta_end)
-        kw["timesteps"] = cs.ddim_timesteps(wl.n_steps, wl.T)
+        kw["abar_table"] = (cs.abar_cosine(wl.T) if wl.schedule == "cosine"
+                            else cs.abar_linear(wl.T, wl.beta_start, wl.beta_end))
+        kw["timesteps"] = cs.timesteps(wl.n_steps, wl.T, wl.spacing)
     if stop_after is not None:
         # run only steps [start, stop_after): emulate an interrupted run
         n_total = wl.n_steps

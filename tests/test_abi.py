@@ -60,6 +60,7 @@ int main(void) {
   F(cfg_sched_state, tau_cap); F(cfg_sched_state, tau1); F(cfg_sched_state, tau2);
   F(cfg_sched_state, decided_at); F(cfg_sched_state, flags); F(cfg_sched_state, min_M);
   F(cfg_sched_state, M); F(cfg_sched_state, G); F(cfg_sched_state, phase);
+  F(cfg_sched_state, pad);
   printf("CFG_TAU_NONE %d\nCFG_SCHED_MAX_STEPS %d\n", CFG_TAU_NONE, CFG_SCHED_MAX_STEPS);
   printf("CFG_SCHED_DEFER %u\nCFG_SCHED_FLAG_DEFER_CLASH %u\n", CFG_SCHED_DEFER, CFG_SCHED_FLAG_DEFER_CLASH);
   return 0;
@@ -74,6 +75,7 @@ int main(void) {
     c = {k: int(v) for k, v in c.items()}
     assert c["cfg_sched_params"] == ctypes.sizeof(cs.SchedParamsC)
     assert c["cfg_sched_state"] == ctypes.sizeof(cs.SchedStateC)
+    assert c["cfg_sched_state"] % 16 == 0          # arrays of states stay 16-byte aligned
     for name, typ in (("cfg_sched_params", cs.SchedParamsC), ("cfg_sched_state", cs.SchedStateC)):
         for field, _ in typ._fields_:
             assert c[f"{name}.{field}"] == getattr(typ, field).offset, (name, field)
@@ -232,3 +234,20 @@ def test_division_by_reciprocal_and_fma_is_correctly_rounded():
             assert F(r) == dF - F(q0) * L          # the residual is exact
             q = float(F(q0) + F(r) * y)
             assert q == d / L, (d, L, q, d / L)
+
+
+def test_adjacent_sampler_tables_match_oracle():
+    """The library's host tables (cosine abar, timestep spacings) equal the oracle's."""
+    for T, s, mb in ((1000, 0.008, 0.999), (10, 0.0, 0.5), (1, 0.1, 0.9)):
+        assert np.array_equal(cs.abar_cosine(T, s, mb), O.abar_cosine(T, s, mb))
+    for N, T in ((50, 1000), (30, 1000), (7, 100), (1, 10), (10, 10)):
+        for sp in ("linspace", "leading", "trailing"):
+            assert np.array_equal(cs.timesteps(N, T, sp), O.timesteps(N, T, sp)), (N, T, sp)
+    out = np.empty(4, dtype=np.int32)
+    p = out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    assert cs.lib.cfg_timesteps(p, 4, 10, 3) == -1                 # unknown spacing
+    assert cs.lib.cfg_timesteps(p, 11, 10, 1) == -1                # n_steps > T
+    d = np.empty(4)
+    pd = d.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+    assert cs.lib.cfg_abar_cosine(pd, 4, -0.1, 0.999) == -1
+    assert cs.lib.cfg_abar_cosine(pd, 4, 0.008, 1.0) == -1

@@ -36,6 +36,10 @@ pytestmark = pytest.mark.gpu
 
 SMALL = [
     ("sd_point_mass_f32", (1, 3, 17, 19)),
+    ("sd_point_mass_f32/cosine/trailing", (1, 4, 16, 16)),
+    ("sdxl_1024_b8_bf16/cosine/linspace", (2, 4, 17, 19)),
+    ("sdxl_1024_b8_bf16/linear/leading", (2, 4, 17, 19)),
+    ("sd_3840px_eta1_bf16/linear/trailing", (1, 4, 29, 31)),
     ("sd_point_mass_f32", (1, 4, 64, 64)),
     ("sdxl_1024_b8_bf16", (3, 4, 17, 19)),
     ("sd_3840px_eta1_bf16", (1, 4, 61, 67)),
@@ -71,9 +75,19 @@ def _perturb(wl):
     return (lambda s, b: W.draw_perturbation(wl, s, b)) if wl.perturb_std else None
 
 
+def _workload(name):
+    """A workload by name; "base/schedule/spacing" selects an adjacent sampler variant."""
+    import dataclasses
+    base, *rest = name.split("/")
+    wl = W.WORKLOADS[base]
+    if rest:
+        wl = dataclasses.replace(wl, schedule=rest[0], spacing=rest[1])
+    return wl
+
+
 @pytest.mark.parametrize("name,shape", SMALL, ids=[f"{n}-{'x'.join(map(str, s))}" for n, s in SMALL])
 def test_small_runs_match_oracle(cuda, name, shape):
-    wl = W.WORKLOADS[name].scaled(shape)
+    wl = _workload(name).scaled(shape)
     inputs = W.draw_inputs(wl)
     gpu = run_workload(wl, inputs, cuda)
     ref = O.run_sampler(wl, inputs, perturb=_perturb(wl))
@@ -198,3 +212,98 @@ def test_callback_error_stops_the_run(cuda):
                        workspace=cs.new_workspace(wl.n, cs.CFG_BF16, cuda),
                        abar_table=cs.abar_linear(), timesteps=cs.ddim_timesteps(wl.n_steps))
     assert seen == [0, 1, 2, 3]
+
+
+@pytest.mark.parametrize("name,shape", [("sdxl_1024_b8_bf16", (2, 4, 32, 32)),
+                                        ("dit_flow_b4_bf16", (1, 16, 24, 24)),
+                                        ("sd_point_mass_f32", (1, 4, 16, 16))])
+def test_sampler_run_captured_in_a_cuda_graph(cuda, name, shape):
+    """A whole run -- every step's denoiser callback and fused step -- recorded into one
+    CUDA graph by stream capture, then replayed twice: x_0 and the schedule state equal the
+    eager run's bit for bit."""
+    from gpu_harness import Denoiser
+    wl = W.WORKLOADS[name].scaled(shape)
+    inputs = W.draw_inputs(wl)
+    eager = run_workload(wl, inputs, cuda)
+    x_T = to_device_stored(inputs["x_T"], wl.dtype, cuda)
+    x = torch.empty_like(x_T)
+    pc, pu = torch.empty_like(x), torch.empty_like(x)
+    ws = cs.new_workspace(wl.n, cs.CFG_F32 if wl.dtype == "f32" else cs.CFG_BF16, cuda)
+    st = cs.new_sched_state(cuda)
+    sp = cs.SchedParams(n_steps=wl.n_steps, L=wl.L, g_slope=wl.g_slope, k=wl.k, tau_cap=wl.tau_cap)
+    kw = dict(mode=cs.CFG_MODE_DDIM if wl.mode == "ddim" else cs.CFG_MODE_FLOW,
+              n_steps=wl.n_steps, w=wl.w, denoise=Denoiser(wl, inputs, x, pc, pu), pred_c=pc,
+              pred_u=pu, sched=sp, state=st, workspace=ws, eta=wl.eta, seed=wl.seed)
+    if wl.mode == "ddim":
+        kw["abar_table"] = cs.abar_linear(wl.T, wl.beta_start, wl.beta_end)
+        kw["timesteps"] = cs.ddim_timesteps(wl.n_steps, wl.T)
+    s = torch.cuda.Stream(cuda)
+    s.wait_stream(torch.cuda.current_stream(cuda))
+    with torch.cuda.stream(s):                     # warm-up outside capture
+        x.copy_(x_T)
+        cs.sampler_run(x, **kw)
+    torch.cuda.current_stream(cuda).wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        x.copy_(x_T)
+        cs.sampler_run(x, **kw)
+    for _ in range(2):
+        x.zero_()
+        st.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(to_host_f64(x), eager.x0)
+        got = cs.read_sched_state(st)
+        assert np.array_equal(got["M"], eager.state["M"])
+        assert np.array_equal(got["G"], eager.state["G"], equal_nan=True)
+        for key in ("n_seen", "tau1p", "argmin", "tau_cap", "tau1", "tau2", "decided_at", "flags"):
+            assert got[key] == eager.state[key], key
+
+
+@pytest.mark.parametrize("name,shape", [("sdxl_1024_b8_bf16", (2, 4, 32, 32)),
+                                        ("sd_3840px_eta1_bf16", (1, 4, 48, 48)),
+                                        ("dit_flow_b4_bf16", (1, 16, 24, 24)),
+                                        ("sd_point_mass_f32", (1, 4, 16, 16))])
+def test_branch_streams_run_equals_single_callback_run(cuda, name, shape):
+    """The CFG-parallel form: the two branches on two streams joined by events before each
+    step give the single-callback run's x_0 and schedule bit for bit."""
+    from gpu_harness import Denoiser
+    wl = W.WORKLOADS[name].scaled(shape)
+    inputs = W.draw_inputs(wl)
+    eager = run_workload(wl, inputs, cuda)
+    x = to_device_stored(inputs["x_T"], wl.dtype, cuda)
+    pc, pu = torch.empty_like(x), torch.empty_like(x)
+    st = cs.new_sched_state(cuda)
+    den = Denoiser(wl, inputs, x, pc, pu)
+    kw = dict(mode=cs.CFG_MODE_DDIM if wl.mode == "ddim" else cs.CFG_MODE_FLOW,
+              n_steps=wl.n_steps, w=wl.w, denoise_branch=den.branch, pred_c=pc, pred_u=pu,
+              stream_c=torch.cuda.Stream(cuda), stream_u=torch.cuda.Stream(cuda),
+              sched=cs.SchedParams(n_steps=wl.n_steps, L=wl.L, g_slope=wl.g_slope, k=wl.k,
+                                   tau_cap=wl.tau_cap),
+              state=st, workspace=cs.new_workspace(wl.n, cs.CFG_F32 if wl.dtype == "f32" else
+                                                   cs.CFG_BF16, cuda),
+              eta=wl.eta, seed=wl.seed)
+    if wl.mode == "ddim":
+        kw["abar_table"] = cs.abar_linear(wl.T, wl.beta_start, wl.beta_end)
+        kw["timesteps"] = cs.ddim_timesteps(wl.n_steps, wl.T)
+    cs.sampler_run_branches(x, **kw)
+    torch.cuda.synchronize()
+    assert den.calls == 2 * wl.n_steps
+    assert np.array_equal(to_host_f64(x), eager.x0)
+    got = cs.read_sched_state(st)
+    assert np.array_equal(got["M"], eager.state["M"])
+    for key in ("tau1p", "tau_cap", "tau1", "tau2", "decided_at", "flags", "n_seen"):
+        assert got[key] == eager.state[key], key
+
+
+def test_branch_streams_must_differ(cuda):
+    x = torch.zeros(64, dtype=torch.bfloat16, device=cuda)
+    s1 = torch.cuda.Stream(cuda)
+    with pytest.raises(cs.CfgError):
+        cs.sampler_run_branches(x, mode=cs.CFG_MODE_FLOW, n_steps=2, w=2.0,
+                                denoise_branch=lambda *a: None, pred_c=x.clone(), pred_u=x.clone(),
+                                stream_c=s1, stream_u=s1, sched=cs.SchedParams(n_steps=2),
+                                state=cs.new_sched_state(cuda),
+                                workspace=cs.new_workspace(64, cs.CFG_BF16, cuda))

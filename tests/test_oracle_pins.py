@@ -396,3 +396,72 @@ def test_harness_rounding_is_fp32_then_bf16():
     assert O._round_pred(v, "bf16")[0] == 1.0
     assert O._round_pred(v, "bf16")[1] == 1.0 + 2.0**-7
     assert O.round_bf16(v)[0] == 1.0 + 2.0**-7   # direct rounding differs (documented)
+
+
+# ---------------------------------------------------------------------------
+# Per-sample rel-MAE (batch-level scale-out)
+# ---------------------------------------------------------------------------
+def test_rel_mae_per_sample_closed_form():
+    """Samples built so that |c - u| = 2^-j_b |u| exactly (u a signed power of two, c = u (1 + 2^-j_b)
+    exact in fp64): each M_b is exactly 2^-j_b, whatever the other samples hold."""
+    g = np.random.default_rng(31)
+    batch, n = 5, 4096
+    js = [1, 3, 7, 12, 20]
+    u = np.ldexp(np.where(g.random((batch, n)) < 0.5, -1.0, 1.0), g.integers(-20, 20, (batch, n)))
+    c = u * (1.0 + np.ldexp(1.0, -np.array(js))[:, None])
+    M = O.rel_mae_per_sample(c.reshape(-1), u.reshape(-1), batch)
+    assert list(M) == [2.0 ** -j for j in js]
+
+
+def test_rel_mae_per_sample_reduces_to_whole_latent():
+    g = np.random.default_rng(32)
+    c, u = g.standard_normal(3000), g.standard_normal(3000)
+    assert O.rel_mae_per_sample(c, u, 1)[0] == O.rel_mae(c, u)
+    # identical samples: every M_b equals the M of one sample (and of the whole batch)
+    cc, uu = np.tile(c[:1000], 3), np.tile(u[:1000], 3)
+    Mb = O.rel_mae_per_sample(cc, uu, 3)
+    assert np.all(Mb == O.rel_mae(c[:1000], u[:1000]))
+    assert abs(O.rel_mae(cc, uu) / Mb[0] - 1) < 1e-14
+
+
+# ---------------------------------------------------------------------------
+# Adjacent samplers: cosine schedule, timestep spacings
+# ---------------------------------------------------------------------------
+def test_cosine_schedule_telescopes_to_f_ratio():
+    """Unclipped, prod_{j<=i} f(j+1)/f(j) telescopes to f(i+1)/f(0); the last beta (f(T) = 0)
+    is clipped to max_beta, so abar_{T-1} = abar_{T-2} (1 - max_beta)."""
+    T, s = 1000, 0.008
+    ab = O.abar_cosine(T, s, 0.999)
+
+    def f(t):
+        return math.cos((t / T + s) / (1 + s) * math.pi / 2) ** 2
+
+    exact = np.array([f(i + 1) / f(0) for i in range(T - 1)])
+    assert np.max(np.abs(ab[:-1] / exact - 1)) < 1e-12
+    assert ab[-1] == ab[-2] * (1 - 0.999)
+    assert np.all(np.diff(ab) < 0) and 0 < ab[-1] < ab[0] < 1
+
+
+def test_timestep_spacings_golden():
+    """Hand-derived sequences (noisiest first)."""
+    assert list(O.timesteps(50, 1000, "trailing")) == [999 - 20 * i for i in range(50)]
+    assert list(O.timesteps(50, 1000, "leading")) == [980 - 20 * i for i in range(50)]
+    assert list(O.timesteps(30, 1000, "trailing")[:4]) == [999, 966, 932, 899]
+    assert list(O.timesteps(30, 1000, "leading")[:3]) == [957, 924, 891]
+    assert list(O.timesteps(30, 1000, "leading")[-1:]) == [0]
+    assert list(O.timesteps(50, 1000, "linspace")[:3]) == [999, 979, 958]
+
+
+@pytest.mark.parametrize("schedule,spacing", [("cosine", "linspace"), ("cosine", "trailing"),
+                                              ("linear", "leading"), ("linear", "trailing")])
+def test_point_mass_run_lands_on_guided_mean_for_any_schedule(schedule, spacing):
+    """Deterministic DDIM with the point-mass denoiser lands on mu* = mu_u + w (mu_c - mu_u) for
+    any abar table and timestep list (the combined epsilon is constant along the run)."""
+    import dataclasses
+    wl = dataclasses.replace(W.WORKLOADS["sd_point_mass_f32"].scaled((1, 4, 8, 8)),
+                             schedule=schedule, spacing=spacing)
+    inputs = W.draw_inputs(wl)
+    r = O.run_sampler(wl, inputs, dtype="f64")
+    mc = inputs["mean_c"].reshape(-1).astype(np.float64)
+    mu = inputs["mean_u"].reshape(-1).astype(np.float64)
+    assert np.max(np.abs(r.x0 - (mu + wl.w * (mc - mu)))) < 1e-11

@@ -77,6 +77,8 @@ class Workload:
     k: int = 10           # tau2 = tau1 + k
     tau_cap: int = -1     # -1: global argmin of the run's own rel-MAE trace
     batch_shared_means: bool = True
+    schedule: str = "linear"      # noise schedule of a DDIM workload: "linear" or "cosine"
+    spacing: str = "linspace"     # DDIM timestep spacing: "linspace", "leading" or "trailing"
 
     @property
     def n(self) -> int:
