@@ -416,7 +416,10 @@ CFG_API int cfg_sampler_run_branches(void* x, int64_t n, int32_t dtype, int32_t 
  * (seed low word, seed high word) and counter (i/4 low, i/4 high, step,
  * stream_id); words (0,1) give elements 4q, 4q+1 as (rho cos, rho sin) with
  * rho = sqrt(-2 ln u0), angle 2 pi u1; words (2,3) likewise give 4q+2, 4q+3;
- * u = (2 (r >> 9) + 1) / 2^24.  The DDIM step uses stream_id 0.
+ * u = (2 (r >> 9) + 1) / 2^24.  The DDIM step uses stream_id 0.  The integer
+ * stream is exact; the transform is evaluated in fp32 (exact integer range
+ * reduction, short series for ln and sin/cos) to within a few fp32 ulps of
+ * the exact values.
  *   out: device float, n elements (n >= 0).
  */
 CFG_API int cfg_randn(float* out, int64_t n, uint64_t seed, uint32_t step, uint32_t stream_id,
