@@ -147,6 +147,62 @@ def test_batched_full_sdxl_run_per_sample_schedules(cuda):
         assert got["n_seen"] == wl.n_steps and got["flags"] == 0
 
 
+def _batched_run(wl, inputs, cuda, batch):
+    """The workload's whole run as a Python loop of batched steps (per-sample schedules,
+    deferred reductions) with the device denoiser; returns (x_0, [state of each sample])."""
+    x = to_device_stored(inputs["x_T"], wl.dtype, cuda)
+    pc, pu = torch.empty_like(x), torch.empty_like(x)
+    den = Denoiser(wl, inputs, x, pc, pu)
+    st = cs.new_sched_state(cuda, batch=batch)
+    sp = cs.SchedParams(n_steps=wl.n_steps, L=wl.L, g_slope=wl.g_slope, k=wl.k, defer=True)
+    ws = cs.new_workspace(wl.n, _code(wl.dtype), cuda, batch=batch)
+    N = wl.n_steps
+    if wl.mode == "ddim":
+        abar = cs.abar_linear(wl.T, wl.beta_start, wl.beta_end)
+        ts = cs.ddim_timesteps(N, wl.T)
+    for s in range(N):
+        if wl.mode == "ddim":
+            ab = float(abar[ts[s]])
+            abp = 1.0 if s == N - 1 else float(abar[ts[s + 1]])
+            den(s, int(ts[s]), ab)
+            cs.ddim_step(x, x, pc, pu, w=wl.w, abar_t=ab, abar_prev=abp, eta=wl.eta, seed=wl.seed,
+                         step=s, state=st, sched=sp, workspace=ws, batch=batch)
+        else:
+            t, tn = 1.0 - s / N, 1.0 - (s + 1) / N
+            den(s, s, t)
+            cs.flow_step(x, x, pc, pu, w=wl.w, t_cur=t, t_next=tn, step=s, state=st, sched=sp,
+                         workspace=ws, batch=batch)
+    torch.cuda.synchronize()
+    return to_host_f64(x), [cs.read_sched_state(st, b) for b in range(batch)]
+
+
+@pytest.mark.parametrize("name,shape", [("dit_flow_b4_bf16", None), ("video_b2_bf16", None),
+                                        ("sd_3840px_eta1_bf16", (3, 4, 64, 64)),
+                                        ("sd_point_mass_f32", (4, 4, 32, 32))])
+def test_batched_whole_runs_per_sample(cuda, name, shape):
+    """Whole runs of the flow, video, eta = 1 and fp32 workloads as batched steps: x_0 within
+    the whole-run tolerance of the oracle, and each sample's M trace and tau values against
+    the oracle's per-sample schedule."""
+    wl = W.WORKLOADS[name] if shape is None else W.WORKLOADS[name].scaled(shape)
+    batch = wl.shape[0]
+    inputs = W.draw_inputs(wl)
+    pert = (lambda s_, b_: W.draw_perturbation(wl, s_, b_)) if wl.perturb_std else None
+    ref = O.run_sampler(wl, inputs, perturb=pert, batch=batch)
+    x0, states = _batched_run(wl, inputs, cuda, batch)
+    if wl.dtype == "f32":
+        assert float(np.max(np.abs(x0 - ref.x0))) <= 1e-5
+        mtol = 1e-6
+    else:
+        assert np.linalg.norm(x0 - ref.x0) <= 2e-2 * np.linalg.norm(ref.x0)
+        assert np.max(np.abs(x0 - ref.x0)) <= 2e-2 * np.max(np.abs(ref.x0))
+        mtol = 1e-3
+    for b, got in enumerate(states):
+        assert np.max(np.abs(got["M"] / ref.M_samples[:, b] - 1)) <= mtol, b
+        assert {k: got[k] for k in ref.sched_samples[b].as_dict()} == ref.sched_samples[b].as_dict(), b
+        assert np.array_equal(got["phase"], ref.sched_samples[b].phase)
+        assert got["n_seen"] == wl.n_steps and got["flags"] == 0
+
+
 def test_batched_arguments_validated(cuda):
     x = torch.zeros(64, dtype=torch.bfloat16, device=cuda)
     ws = cs.new_workspace(64, cs.CFG_BF16, cuda, batch=2)

@@ -426,3 +426,50 @@ def test_in_launch_call_completes_pending_step(cuda):
     torch.cuda.synchronize()
     assert abs(M0.item() / O.rel_mae(d["c64"], d["u64"]) - 1) <= 1e-6
     assert abs(M1.item() / O.rel_mae(d["x64"], d["u64"]) - 1) <= 1e-6
+
+
+def test_step_beyond_2_31_elements(cuda):
+    """One bf16 step over n = 2^31 + 13 elements (64-bit indexing; ~17 GB of HBM).  M is known
+    exactly by construction (u = +-2^k, c = u (1 + 2^-4) is exact in bf16, so every
+    |c - u| = 2^-4 |u| and M = 2^-4); x_out is checked against the oracle's update on sampled
+    elements, including both sides of 2^31 and the ragged tail, with eta = 1 noise."""
+    free, _ = torch.cuda.mem_get_info(cuda)
+    n = 2**31 + 13
+    if free < 4 * 2 * n + (2 << 30):
+        pytest.skip("needs ~18 GB of free device memory")
+    g = torch.Generator(device=cuda)
+    g.manual_seed(123)
+    x = torch.empty(n, dtype=torch.bfloat16, device=cuda)
+    u = torch.empty_like(x)
+    chunk = 1 << 28
+    for i0 in range(0, n, chunk):
+        m = min(chunk, n - i0)
+        x[i0:i0 + m] = torch.randn(m, generator=g, device=cuda).to(torch.bfloat16)
+        e = torch.randint(-6, 6, (m,), generator=g, device=cuda).float()
+        sgn = torch.randint(0, 2, (m,), generator=g, device=cuda).float() * 2 - 1
+        u[i0:i0 + m] = (sgn * torch.exp2(e)).to(torch.bfloat16)
+    c = torch.empty_like(u)
+    for i0 in range(0, n, chunk):
+        m = min(chunk, n - i0)
+        c[i0:i0 + m] = (u[i0:i0 + m].float() * (1.0 + 2.0**-4)).to(torch.bfloat16)
+    out = torch.empty_like(x)
+    M = torch.zeros(1, dtype=torch.float64, device=cuda)
+    abar = O.abar_linear()
+    ab, abp = float(abar[300]), float(abar[280])
+    cs.ddim_step(out, x, c, u, w=5.0, abar_t=ab, abar_prev=abp, eta=1.0, seed=77, step=4, M_out=M,
+                 workspace=cs.new_workspace(n, cs.CFG_BF16, cuda))
+    torch.cuda.synchronize()
+    assert abs(M.item() - 2.0**-4) <= 1e-6 * 2.0**-4
+    rng = np.random.default_rng(5)
+    idx = np.unique(np.concatenate([rng.integers(0, n, 2000), np.arange(2**31 - 40, 2**31 + 13),
+                                    np.arange(n - 20, n), np.arange(0, 20)]))
+    it = torch.from_numpy(idx).to(cuda)
+    xs, cs_, us, got = (t[it].float().cpu().numpy().astype(np.float64) for t in (x, c, u, out))
+    z = np.array([O.gaussian_noise(1, 77, 4, start=int(i))[0] for i in idx])
+    ref, _ = O.ddim_step(xs, cs_, us, "bf16", 5.0, ab, abp, 1.0, 77, 4, z=z)
+    assert np.max(np.abs(got - ref) / np.maximum(np.abs(ref), 1.0)) <= 2e-2
+    # every sampled element within 1 bf16 ulp, or 2^-17 after cancellation (the single-step bound)
+    ok = (ulp_distance_bf16(got, ref) <= 1) | (np.abs(got - ref) <= 2.0**-17)
+    assert ok.all(), idx[~ok][:10]
+    del x, u, c, out
+    torch.cuda.empty_cache()
