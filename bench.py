@@ -13,7 +13,10 @@ Prints ONE JSON line (rank 0):
   e2e                the same metric through the public Python API with pinned host
                      buffers, host->device and device->host copies inside the timed region
   cpu_baseline       the CPU oracle timed on a bounded sample (rank 0, N = 1)
-  sweep              the same device measurement on every other workload (rank 0, N = 1)
+  sweep              the same device measurement on every other workload, and the default
+                     workload as a batched call with a schedule per sample (rank 0, N = 1)
+  sampler_run        whole 50-step runs through the public API with a synthetic denoiser:
+                     eager host loop, captured CUDA graph, two branch streams (rank 0, N = 1)
 
 ``--impl reference`` times the CPU oracle instead (the slow reference program)
 and prints the same kind of line with ``"impl": "reference"``.
@@ -313,9 +316,12 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
     barrier(world)
     ms = start.elapsed_time(end)
     state = cs.read_sched_state(st)
+    # launches in the timed region: every step, plus a flush ending each graph of a partial run
+    def graph_launches(count):
+        return count + (1 if count % wl.n_steps else 0) if count else 0
+    launches = full_reps * graph_launches(G) + graph_launches(rem)
     return {"ms": ms, "n_sets": n_sets, "set_bytes": set_bytes, "l2_bytes": l2,
-            "graph_steps": G, "launches": steps + (1 if steps % wl.n_steps else 0),
-            "state_flags": state["flags"]}
+            "graph_steps": G, "launches": launches, "state_flags": state["flags"]}
 
 
 def time_e2e(wl: W.Workload, steps: int, device, depth: int = 3):
