@@ -540,6 +540,42 @@ def oracle_threads() -> int:
     return 1
 
 
+def time_randn(n: int, launches: int, warmup: int, device):
+    """The eta noise alone: `launches` cfg_randn calls of n normals, replayed from CUDA graphs.
+
+    The step kernel draws the same Philox4x32-10 + Box-Muller stream in registers; this
+    isolates its ALU cost (the output is 4n bytes, written once per launch).
+    """
+    import torch
+    import cfg_guided_sampler_step_b300 as cs
+    out = torch.empty(max(n, 1), dtype=torch.float32, device=device)
+    G = max(1, min(100, launches))
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        for j in range(warmup):
+            cs.randn(out[:n], seed=7, step=j, stream=s)
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for j in range(G):
+            cs.randn(out[:n], seed=7, step=j, stream=s)
+    reps = max(1, launches // G)
+    with torch.cuda.stream(s):
+        g.replay()
+    torch.cuda.synchronize(device)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):              # a graph replays on the current stream
+        ev0.record(s)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(s)
+    ev1.synchronize()
+    us = ev0.elapsed_time(ev1) * 1e3 / (reps * G)
+    return {"kernel": "randn_kernel", "normals": n, "launches": reps * G, "us_per_launch": us,
+            "g_normals_per_s": n / us * 1e-3}
+
+
 # ---------------------------------------------------------------------------
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
@@ -555,6 +591,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--sets", type=int, default=None,
                     help="buffer sets to rotate over (default: >= 4x L2); fewer only for profiling")
+    ap.add_argument("--randn", type=int, default=None, metavar="N",
+                    help="time only the eta-noise stream (cfg_randn, N normals per launch) and exit")
     args = ap.parse_args(argv)
     world, rank, local = dist_env()
     wl = W.WORKLOADS[args.workload]
@@ -589,6 +627,10 @@ def main(argv=None):
     device = torch.device("cuda", local)
     dist_init(world, "nccl")
     import cfg_guided_sampler_step_b300 as cs  # noqa: F401  (fails loudly if not built)
+    if args.randn is not None:
+        if rank == 0:
+            print(json.dumps(time_randn(args.randn, args.steps, warmup, device)), flush=True)
+        return 0
 
     uuid = None
     try:

@@ -410,6 +410,75 @@ def test_deferred_same_parity_clash_is_flagged(cuda):
     assert got["flags"] & cs.SCHED_FLAG_OUT_OF_ORDER     # step 2 recorded after step 0 was dropped
 
 
+def test_deferred_results_lag(cuda):
+    """In a run of deferring steps, step s's M is written by step s + 1's launch and its schedule
+    update by step s + 2's: after steps 0..k, M[0..k-1] are final, M[k] is pending and the rule
+    has seen steps 0..k-2, until a flush completes both."""
+    N, k = 10, 5
+    n = 50_000
+    preds = [_inputs(n, "bf16", seed=600 + s, cuda=cuda) for s in range(k + 1)]
+    ws = cs.new_workspace(n, cs.CFG_BF16, cuda)
+    st = cs.new_sched_state(cuda)
+    sp = cs.SchedParams(n_steps=N, L=2, g_slope=0.01, k=3, defer=True)
+    Ms = torch.full((k + 1,), -1.0, dtype=torch.float64, device=cuda)
+    out = torch.empty_like(preds[0]["x"])
+    ab, abp = float(O.abar_linear()[900]), float(O.abar_linear()[880])
+    for s in range(k + 1):
+        cs.ddim_step(out, preds[s]["x"], preds[s]["c"], preds[s]["u"], w=3.0, abar_t=ab,
+                     abar_prev=abp, step=s, M_out=Ms[s:s + 1], state=st, sched=sp, workspace=ws)
+    torch.cuda.synchronize()
+    M = Ms.cpu().numpy()
+    refs = [O.rel_mae(p["c64"], p["u64"]) for p in preds]
+    for s in range(k):
+        assert abs(M[s] / refs[s] - 1) <= 1e-6, s
+    assert M[k] == -1.0
+    assert cs.read_sched_state(st)["n_seen"] == k - 1
+    cs.workspace_flush(ws)
+    torch.cuda.synchronize()
+    M = Ms.cpu().numpy()
+    assert all(abs(M[s] / refs[s] - 1) <= 1e-6 for s in range(k + 1))
+    got = cs.read_sched_state(st)
+    assert got["n_seen"] == k + 1 and got["flags"] == 0
+
+
+def test_reduce_call_mid_run_completes_pending_steps(cuda):
+    """A rel-MAE call on the same workspace in the middle of a deferred run completes the pending
+    work (the last step's reduction and the schedule update before it); the run then goes on
+    and ends with the synchronous run's results and state."""
+    N, n = 8, 40_003
+    preds = [_inputs(n, "bf16", seed=700 + s, cuda=cuda) for s in range(N)]
+    abar = O.abar_linear()
+    ts = O.ddim_timesteps(N)
+
+    def run(defer, interrupt):
+        x = preds[0]["x"].clone()
+        Mbuf = torch.full((N,), -1.0, dtype=torch.float64, device=cuda)
+        Mr = torch.full((1,), -1.0, dtype=torch.float64, device=cuda)
+        st = cs.new_sched_state(cuda)
+        sp = cs.SchedParams(n_steps=N, L=2, g_slope=0.01, k=3, defer=defer)
+        ws = cs.new_workspace(n, cs.CFG_BF16, cuda)
+        for s in range(N):
+            abp = 1.0 if s == N - 1 else float(abar[ts[s + 1]])
+            cs.ddim_step(x, x, preds[s]["c"], preds[s]["u"], w=4.0, abar_t=float(abar[ts[s]]),
+                         abar_prev=abp, eta=0.0, seed=9, step=s, M_out=Mbuf[s:s + 1], state=st,
+                         sched=sp, workspace=ws)
+            if interrupt and s == 3:
+                cs.relmae_reduce(preds[0]["c"], preds[0]["u"], M_out=Mr, workspace=ws)
+                torch.cuda.synchronize()
+                assert np.all(Mbuf[:4].cpu().numpy() >= 0)      # steps 0..3 all complete
+                assert cs.read_sched_state(st)["n_seen"] == 4
+                assert abs(Mr.item() / O.rel_mae(preds[0]["c64"], preds[0]["u64"]) - 1) <= 1e-6
+        torch.cuda.synchronize()
+        return x.clone(), Mbuf.cpu().numpy(), cs.read_sched_state(st)
+
+    xs, Ms, sts = run(False, False)
+    xd, Md, std = run(True, True)
+    assert torch.equal(xs, xd) and np.array_equal(Ms, Md)
+    for key in ("n_seen", "tau1p", "argmin", "tau_cap", "tau1", "tau2", "decided_at", "flags"):
+        assert sts[key] == std[key], key
+    assert np.array_equal(sts["M"], std["M"]) and np.array_equal(sts["phase"], std["phase"])
+
+
 def test_in_launch_call_completes_pending_step(cuda):
     n = 40_000
     d = _inputs(n, "f32", seed=47, cuda=cuda)
