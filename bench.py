@@ -205,16 +205,17 @@ def step_plan(wl: W.Workload, cs):
     return [dict(step=s, t_cur=1.0 - s / N, t_next=1.0 - (s + 1) / N) for s in range(N)]
 
 
-def enqueue_step(cs, wl, bufs, plan_s, ws, st, sp, M=None, batch=1):
+def enqueue_step(cs, wl, bufs, plan_s, ws, st, sp, M=None, batch=1, stream=None):
     x, pc, pu = bufs[:3]
     xo = bufs[3] if len(bufs) > 3 else x
     if wl.mode == "ddim":
         cs.ddim_step(xo, x, pc, pu, w=wl.w, abar_t=plan_s["abar_t"], abar_prev=plan_s["abar_prev"],
                      eta=wl.eta, seed=wl.seed, step=plan_s["step"], M_out=M, state=st, sched=sp,
-                     workspace=ws, batch=batch)
+                     workspace=ws, batch=batch, stream=stream)
     else:
         cs.flow_step(xo, x, pc, pu, w=wl.w, t_cur=plan_s["t_cur"], t_next=plan_s["t_next"],
-                     step=plan_s["step"], M_out=M, state=st, sched=sp, workspace=ws, batch=batch)
+                     step=plan_s["step"], M_out=M, state=st, sched=sp, workspace=ws, batch=batch,
+                     stream=stream)
 
 
 def make_sets(wl, n_sets, device, torch):
@@ -338,9 +339,12 @@ def time_e2e(wl: W.Workload, steps: int, device, depth: int = 3):
     inp = W.draw_prediction_pair(wl.n, wl.dtype, wl.seed)
 
     def host(a):
+        # page-locked buffers from the library's host allocator (cfg_host_alloc)
         t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
         t = t.view(dt) if a.dtype == np.uint16 else t
-        return t.pin_memory()
+        h = cs.pinned_empty(t.numel(), dt)
+        h.copy_(t)
+        return h
 
     hx, hc, hu = host(inp["x"]), host(inp["c"]), host(inp["u"])
     slots = []
@@ -348,8 +352,8 @@ def time_e2e(wl: W.Workload, steps: int, device, depth: int = 3):
         dx = torch.empty(wl.n, dtype=dt, device=device)
         slots.append(dict(x=dx, c=torch.empty_like(dx), u=torch.empty_like(dx),
                           M=torch.zeros(1, dtype=torch.float64, device=device),
-                          hout=torch.empty(wl.n, dtype=dt).pin_memory(),
-                          hM=torch.empty(1, dtype=torch.float64).pin_memory(),
+                          hout=cs.pinned_empty(wl.n, dt),
+                          hM=cs.pinned_empty(1, torch.float64),
                           ev_in=torch.cuda.Event(), ev_run=torch.cuda.Event(),
                           ev_out=torch.cuda.Event(), used=False))
     ws = cs.new_workspace(wl.n, cs.CFG_F32 if wl.dtype == "f32" else cs.CFG_BF16, device)
@@ -359,26 +363,24 @@ def time_e2e(wl: W.Workload, steps: int, device, depth: int = 3):
                         defer=False)
     plan = step_plan(wl, cs)
     s_in, s_run, s_out = (torch.cuda.Stream(device) for _ in range(3))
+    h_in, h_run, h_out = s_in.cuda_stream, s_run.cuda_stream, s_out.cuda_stream
 
     def one(i):
         sl = slots[i % depth]
-        with torch.cuda.stream(s_in):
-            if sl["used"]:
-                s_in.wait_event(sl["ev_out"])         # the slot's last result is on the host
-            sl["x"].copy_(hx, non_blocking=True)
-            sl["c"].copy_(hc, non_blocking=True)
-            sl["u"].copy_(hu, non_blocking=True)
-            sl["ev_in"].record(s_in)
-        with torch.cuda.stream(s_run):
-            s_run.wait_event(sl["ev_in"])
-            enqueue_step(cs, wl, (sl["x"], sl["c"], sl["u"]), plan[i % wl.n_steps], ws, st, sp,
-                         M=sl["M"])
-            sl["ev_run"].record(s_run)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(sl["ev_run"])
-            sl["hout"].copy_(sl["x"], non_blocking=True)
-            sl["hM"].copy_(sl["M"], non_blocking=True)
-            sl["ev_out"].record(s_out)
+        if sl["used"]:
+            s_in.wait_event(sl["ev_out"])             # the slot's last result is on the host
+        cs.copy_async(sl["x"], hx, stream=h_in)
+        cs.copy_async(sl["c"], hc, stream=h_in)
+        cs.copy_async(sl["u"], hu, stream=h_in)
+        sl["ev_in"].record(s_in)
+        s_run.wait_event(sl["ev_in"])
+        enqueue_step(cs, wl, (sl["x"], sl["c"], sl["u"]), plan[i % wl.n_steps], ws, st, sp,
+                     M=sl["M"], stream=h_run)
+        sl["ev_run"].record(s_run)
+        s_out.wait_event(sl["ev_run"])
+        cs.copy_async(sl["hout"], sl["x"], stream=h_out)
+        cs.copy_async(sl["hM"], sl["M"], stream=h_out)
+        sl["ev_out"].record(s_out)
         sl["used"] = True
 
     for i in range(2 * depth):
@@ -389,16 +391,20 @@ def time_e2e(wl: W.Workload, steps: int, device, depth: int = 3):
     start.record(s_in)
     s_run.wait_event(start)
     s_out.wait_event(start)
+    t0 = time.perf_counter()
     for i in range(steps):
         one(i)
     end.record(s_out)
+    host_s = time.perf_counter() - t0
     end.synchronize()
     torch.cuda.synchronize(device)
     ms = start.elapsed_time(end)
     eb = wl.elem_bytes
     return {"value": wl.n * steps / (ms * 1e-3), "unit": "latent elements/s",
             "h2d_bytes_per_step": 3 * wl.n * eb, "d2h_bytes_per_step": wl.n * eb + 8,
-            "steps": steps, "ms_per_step": ms / steps, "pipeline_depth": depth}
+            "steps": steps, "ms_per_step": ms / steps, "pipeline_depth": depth,
+            "host_enqueue_us_per_step": host_s * 1e6 / steps,
+            "host_buffers": "page-locked (cfg_host_alloc), copies by cfg_copy_async"}
 
 
 def time_sampler_runs(wl: W.Workload, device, runs: int = 20):
@@ -671,7 +677,9 @@ def main(argv=None):
                 "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
                 "us_per_step": e2e["ms_per_step"] * 1e3,
                 "pipeline": f"{e2e['pipeline_depth']} buffer slots; upload, step and download "
-                            "streams ordered by events"},
+                            "streams ordered by events",
+                "host_buffers": e2e["host_buffers"],
+                "host_enqueue_us_per_step": e2e["host_enqueue_us_per_step"]},
         "gpu_launches": dev["launches"],
         "clocks": clk,
     }

@@ -7,7 +7,8 @@
 // sections 1 and 3), and the adjacent samplers it names (a cosine schedule,
 // fewer spaced steps).  Loops: a whole CFG sampler run, with the two branch
 // predictions from one callback or from two streams (the CFG-parallel form of
-// the xDiT review, section 3).
+// the xDiT review, section 3).  Page-locked host buffers for the copies around
+// a step.
 
 #include <cuda_runtime.h>
 
@@ -31,6 +32,34 @@ int check_dtype(int32_t dtype) {
 }  // namespace
 
 extern "C" {
+
+CFG_API int cfg_host_alloc(size_t bytes, void** out) {
+  if (out == nullptr) return fail(CFG_ERR_INVALID_ARG, "out must not be NULL");
+  *out = nullptr;
+  if (bytes == 0) return fail(CFG_ERR_INVALID_ARG, "bytes must be >= 1");
+  const cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocPortable);
+  if (e != cudaSuccess) {
+    *out = nullptr;
+    return cuda_fail(e, "cudaHostAlloc");
+  }
+  return CFG_OK;
+}
+
+CFG_API int cfg_host_free(void* p) {
+  if (p == nullptr) return CFG_OK;
+  const cudaError_t e = cudaFreeHost(p);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFreeHost");
+  return CFG_OK;
+}
+
+CFG_API int cfg_copy_async(void* dst, const void* src, size_t bytes, void* stream) {
+  if (bytes == 0) return CFG_OK;
+  if (dst == nullptr || src == nullptr) return fail(CFG_ERR_INVALID_ARG, "dst and src must not be NULL");
+  const cudaError_t e =
+      cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+  return CFG_OK;
+}
 
 CFG_API int cfg_abar_linear(double* abar_out, int32_t T, double beta_start, double beta_end) {
   if (abar_out == nullptr) return fail(CFG_ERR_INVALID_ARG, "abar_out must not be NULL");

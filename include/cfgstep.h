@@ -460,6 +460,30 @@ enum cfg_spacing { CFG_SPACING_LINSPACE = 0, CFG_SPACING_LEADING = 1, CFG_SPACIN
 CFG_API int cfg_abar_cosine(double* abar_out, int32_t T, double s, double max_beta);
 CFG_API int cfg_timesteps(int32_t* out, int32_t n_steps, int32_t T, int32_t spacing);
 
+/*
+ * Page-locked host memory for the host<->device copies around a step
+ * (cudaHostAlloc, portable to every device).  A step whose inputs and
+ * results live in host memory copies 4n elements per step; from buffers
+ * allocated here those copies run asynchronously at the link's rate.
+ *   cfg_host_alloc: bytes >= 1; *out receives the pointer (host memory,
+ *     owned by the caller until cfg_host_free); CFG_ERR_CUDA if the
+ *     allocation fails (*out is then NULL).
+ *   cfg_host_free: p from cfg_host_alloc, or NULL (a no-op).
+ */
+CFG_API int cfg_host_alloc(size_t bytes, void** out);
+CFG_API int cfg_host_free(void* p);
+
+/*
+ * Asynchronous copy of `bytes` bytes between any two of host and device
+ * memory (cudaMemcpyAsync, direction from the pointers) on `stream`.  With a
+ * page-locked host side (cfg_host_alloc) it returns at once and the copy
+ * runs in stream order, overlapping other streams' work; with pageable host
+ * memory the driver stages it and the call may block.
+ *   dst, src: non-NULL unless bytes == 0 (then a no-op); the ranges must not
+ *   overlap.  CFG_ERR_CUDA if the runtime rejects the copy.
+ */
+CFG_API int cfg_copy_async(void* dst, const void* src, size_t bytes, void* stream);
+
 /* Message of the last failed call on this host thread ("" if none). */
 CFG_API const char* cfg_last_error(void);
 
