@@ -328,11 +328,9 @@ class _HostBlock:
 def pinned_empty(numel: int, dtype) -> "torch.Tensor":
     """A CPU tensor of `numel` elements on page-locked memory from cfg_host_alloc.
 
-    Host<->device copies from/to it (``copy_(..., non_blocking=True)``) run asynchronously at
-    the link's rate; on the virtualised hosts this library is measured on, such buffers move
-    data about four times faster than tensors pinned by torch's own host allocator.  (torch's
-    ``is_pinned()`` reports only its own pool, so it says False here; the driver knows the
-    memory is page-locked.)
+    Copies from/to it with :func:`copy_async` run asynchronously in stream order.  (torch's
+    ``is_pinned()`` reports only its own pool, so it says False here, and ``Tensor.copy_``
+    treats the memory as pageable; the driver knows it is page-locked.)
     """
     torch = _torch()
     itemsize = torch.empty((), dtype=dtype).element_size()

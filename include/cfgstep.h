@@ -464,7 +464,7 @@ CFG_API int cfg_timesteps(int32_t* out, int32_t n_steps, int32_t T, int32_t spac
  * Page-locked host memory for the host<->device copies around a step
  * (cudaHostAlloc, portable to every device).  A step whose inputs and
  * results live in host memory copies 4n elements per step; from buffers
- * allocated here those copies run asynchronously at the link's rate.
+ * allocated here those copies run asynchronously (cfg_copy_async).
  *   cfg_host_alloc: bytes >= 1; *out receives the pointer (host memory,
  *     owned by the caller until cfg_host_free); CFG_ERR_CUDA if the
  *     allocation fails (*out is then NULL).
