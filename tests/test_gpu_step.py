@@ -180,6 +180,64 @@ def test_relmae_degenerate_cases(cuda):
     assert math.isnan(M.item())
 
 
+def _with_inf(arr, dtype, positions, sign=1.0):
+    """A copy of a stored array with +-inf at `positions` (storage form)."""
+    out = np.array(arr, copy=True)
+    if dtype == "f32":
+        out[positions] = sign * np.inf
+    else:
+        out[positions] = 0x7F80 if sign > 0 else 0xFF80      # bf16 +-inf bits
+    return out
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("mode", ["ddim0", "ddim1", "flow", "reduce"])
+def test_infinite_predictions(cuda, dtype, mode):
+    """An infinite conditional prediction (u finite) makes the L1 sum infinite, so M = +inf as in
+    the oracle; an infinite unconditional one makes M = inf/inf = NaN.  Elements away from the
+    infinities match the oracle as usual; at them both sides are non-finite (the update's
+    combined coefficients give +-inf where the pages' two-term DDIM form gives inf - inf = NaN)."""
+    n = 70_003
+    base = W.draw_prediction_pair(n, dtype, 77)
+    pos = [5, 4096 * 3 + 1, n - 2]                  # vector path and ragged tail
+    ab, abp = float(O.abar_linear()[600]), float(O.abar_linear()[580])
+    ws = cs.new_workspace(n, _code(dtype), cuda)
+    for which, sign, want in (("c", 1.0, "inf"), ("c", -1.0, "inf"), ("u", 1.0, "nan")):
+        arrs = dict(base)
+        arrs[which] = _with_inf(base[which], dtype, pos, sign)
+        dev = {k: to_device_stored(arrs[k], dtype, cuda) for k in ("x", "c", "u")}
+        f64 = {k: W.stored_to_f64(arrs[k], dtype) for k in ("x", "c", "u")}
+        M = torch.zeros(1, dtype=torch.float64, device=cuda)
+        out = torch.empty_like(dev["x"])
+        with np.errstate(invalid="ignore", over="ignore"):     # the oracle's inf - inf
+            if mode == "reduce":
+                cs.relmae_reduce(dev["c"], dev["u"], M_out=M, workspace=ws)
+                refM, ref = O.rel_mae(f64["c"], f64["u"]), None
+            elif mode == "flow":
+                cs.flow_step(out, dev["x"], dev["c"], dev["u"], w=3.5, t_cur=0.5, t_next=0.45,
+                             M_out=M, workspace=ws)
+                ref, refM = O.flow_step(f64["x"], f64["c"], f64["u"], dtype, 3.5, 0.5, 0.45)
+            else:
+                eta = 1.0 if mode == "ddim1" else 0.0
+                cs.ddim_step(out, dev["x"], dev["c"], dev["u"], w=7.5, abar_t=ab, abar_prev=abp,
+                             eta=eta, seed=5, step=3, M_out=M, workspace=ws)
+                ref, refM = O.ddim_step(f64["x"], f64["c"], f64["u"], dtype, 7.5, ab, abp, eta,
+                                        5, 3)
+        torch.cuda.synchronize()
+        got_M = M.item()
+        if want == "inf":
+            assert got_M == math.inf and refM == math.inf
+        else:
+            assert math.isnan(got_M) and math.isnan(refM)
+        if ref is None:
+            continue
+        got = to_host_f64(out)
+        fin = np.isfinite(ref)
+        assert not fin[pos].any() and not np.isfinite(got[pos]).any()
+        assert np.isfinite(got[fin]).all()
+        _compare(got[fin], ref[fin], dtype, strict_ulp=(mode != "ddim1"))
+
+
 def test_identical_branches_ignore_w(cuda):
     n = 10_001
     d = _inputs(n, "bf16", seed=13, cuda=cuda)
