@@ -227,6 +227,20 @@ def test_rel_mae_degenerate_cases():
     assert math.isnan(O.rel_mae(np.array([math.nan, 1.0]), np.array([1.0, 1.0])))
 
 
+def test_rel_mae_non_finite_predictions():
+    """IEEE arithmetic on the definition: an infinite conditional prediction gives an infinite
+    numerator (M = +inf, also over an all-zero denominator); an infinite unconditional one makes
+    both sums infinite (inf/inf = NaN); both infinite at one element gives inf - inf = NaN."""
+    inf = math.inf
+    one = np.ones(4)
+    with np.errstate(invalid="ignore"):
+        assert O.rel_mae(np.array([inf, 1, 1, 1.0]), one) == inf
+        assert O.rel_mae(np.array([-inf, 1, 1, 1.0]), one) == inf
+        assert O.rel_mae(np.array([inf, 0, 0, 0.0]), np.zeros(4)) == inf
+        assert math.isnan(O.rel_mae(one, np.array([inf, 1, 1, 1.0])))
+        assert math.isnan(O.rel_mae(np.array([inf, 1, 1, 1.0]), np.array([inf, 1, 1, 1.0])))
+
+
 def test_guidance_special_cases():
     g = np.random.default_rng(11)
     c, u = g.standard_normal(100), g.standard_normal(100)
