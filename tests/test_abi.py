@@ -10,6 +10,7 @@ from pathlib import Path
 
 import numpy as np
 import pytest
+import torch
 
 import cfg_guided_sampler_step_b300 as cs
 from oracle import cfg_oracle as O
@@ -184,6 +185,22 @@ def test_other_entry_points_validate():
     assert L.cfg_abar_linear(out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), 4, 0.1, 1.5) == -1
     ts = np.empty(4, dtype=np.int32)
     assert L.cfg_ddim_timesteps(ts.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), 5, 4) == -1
+
+
+def test_host_buffer_helpers_validate():
+    """cfg_host_alloc / cfg_host_free / cfg_copy_async reject bad arguments before any CUDA call
+    (so this runs without a GPU)."""
+    ptr = ctypes.c_void_p(1)
+    assert cs.lib.cfg_host_alloc(0, ctypes.byref(ptr)) == -1 and ptr.value is None
+    assert cs.lib.cfg_host_alloc(16, None) == -1
+    assert cs.lib.cfg_host_free(None) == 0
+    assert cs.lib.cfg_copy_async(None, None, 0, None) == 0          # zero bytes: nothing to do
+    assert cs.lib.cfg_copy_async(None, FAKE, 16, None) == -1
+    assert cs.lib.cfg_copy_async(FAKE, None, 16, None) == -1
+    with pytest.raises(ValueError):
+        cs.copy_async(torch.empty(4), torch.empty(5))               # sizes differ
+    with pytest.raises(ValueError):
+        cs.copy_async(torch.empty(4, 2).t(), torch.empty(8))        # not contiguous
 
 
 def test_sampler_run_validates_before_any_callback():
