@@ -198,7 +198,8 @@ CFG_API int cfg_workspace_flush(void* ws, size_t ws_bytes, void* stream);
  * rel-MAE alone (Hybridiff notes, key design 2; with the velocity pair for
  * flow models, "Loss / training strategy"):
  *   M = sum_i |pred_c[i] - pred_u[i]| / sum_i |pred_u[i]|
- * with 0/0 -> 0 and x/0 -> +inf.
+ * with 0/0 -> 0 and x/0 -> +inf; otherwise IEEE: an infinite prediction
+ * makes its sum +inf (so M = +inf, or NaN for inf/inf), and a NaN makes M NaN.
  *   pred_c, pred_u  device, n elements of dtype;
  *   M_out           device double, nullable: receives M;
  *   st, sp          nullable together: when given, M is recorded as step
