@@ -254,20 +254,25 @@ CFG_API int cfg_ddim_step(void* x_out, const void* x_in, const void* pred_c, con
  *
  * Arguments, results and errors are those of cfg_ddim_step, minus ws and
  * ws_bytes.  The scratch is one static device array inside this library of
- * cfg_workspace_bytes() = 196,864 bytes, held by every GPU that loads the
- * library until the process exits.  It covers any n: the grid never exceeds
- * the 4096 block partials the array holds; a request that would need more
- * is rejected with CFG_ERR_WORKSPACE.  CFG_SCHED_DEFER is rejected
+ * cfg_workspace_bytes() = 196,864 bytes (the maximum: one workspace), held
+ * by every GPU that loads the library until the process exits.  No n needs
+ * more: the streaming grid is capped at the 4096 block partials one
+ * workspace holds, so no size is rejected for want of scratch (n < 0 is
+ * rejected as by cfg_ddim_step).  CFG_SCHED_DEFER is rejected
  * (CFG_ERR_INVALID_ARG): every call finishes its rel-MAE in-launch.
- *   - No allocation: the call uses no cudaMalloc, cudaFree or allocating
- *     library routine.
+ *   - No allocation: the call uses no cudaMalloc, cudaFree, memset or
+ *     allocating library routine.
  *   - Set-up: the first call on each device (with that device current) looks
- *     up the array's device address and zeroes its 256-byte header with a
- *     synchronous cudaMemset; make that first call before any stream capture.
+ *     up the array's device address with cudaGetSymbolAddress and caches it
+ *     (safe when several host threads make their first call at once); make
+ *     that first call before any stream capture.  Nothing is written: the
+ *     array is zero when the library's device code loads, and every call
+ *     leaves its header (completion counter, no pending work) as it found it.
  *   - Sharing: all calls on a device share the one array, which keeps the
  *     last call's contents.  Calls that may overlap on the GPU (different
  *     streams, or host threads without ordering) race on it: serialise them
- *     on one stream.
+ *     on one stream.  Calls in a row on one stream are ordered and may be
+ *     issued without host synchronisation between them.
  */
 CFG_API int cfg_ddim_step_static_ws(void* x_out, const void* x_in, const void* pred_c,
                                     const void* pred_u, int64_t n, int32_t dtype, float w,

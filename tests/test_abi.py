@@ -1,7 +1,9 @@
 """The C ABI without a GPU: exports, struct layout, argument validation, host helpers.
 
-No call here reaches the CUDA runtime: every invalid call is rejected by the
-library's host-side checks before any launch.
+No call here launches anything: every invalid call is rejected by the library's
+host-side checks, and the one test that passes validation (first calls from
+several host threads) runs only where no CUDA device exists, so the library's
+device lookup is the call that fails.
 """
 import ctypes
 import re
@@ -268,3 +270,42 @@ def test_adjacent_sampler_tables_match_oracle():
     pd = d.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
     assert cs.lib.cfg_abar_cosine(pd, 4, -0.1, 0.999) == -1
     assert cs.lib.cfg_abar_cosine(pd, 4, 0.008, 1.0) == -1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on fake pointers")
+def test_first_calls_from_many_threads_without_a_device():
+    """Calls that pass argument validation reach the library's per-device lookups (SM count,
+    static scratch address).  Made at once from several host threads with no device present,
+    each must fail cleanly with CFG_ERR_CUDA and its own thread's message; the lookups are
+    atomic, so concurrent first calls neither crash nor leave a bad cached value."""
+    import threading
+    sp = cs.SchedParams(n_steps=4)
+    fake = 1 << 20                      # 16-byte aligned, never dereferenced on the host
+    results = []
+    lock = threading.Lock()
+    start = threading.Barrier(8)
+
+    def worker(i):
+        start.wait()
+        for _ in range(50):
+            if i % 2:
+                rc = cs.lib.cfg_ddim_step(fake, fake, fake, fake, 1024, cs.CFG_BF16, 2.0, 0.5, 0.6,
+                                          0.0, 0, 0, None, fake, ctypes.byref(sp.c), fake,
+                                          cs.workspace_bytes(1024, cs.CFG_BF16), None)
+            else:
+                rc = cs.lib.cfg_ddim_step_static_ws(fake, fake, fake, fake, 1024, cs.CFG_BF16, 2.0,
+                                                    0.5, 0.6, 0.0, 0, 0, None, fake,
+                                                    ctypes.byref(sp.c), None)
+            msg = cs.lib.cfg_last_error().decode()
+            with lock:
+                results.append((rc, msg))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(60)
+    assert len(results) == 8 * 50
+    for rc, msg in results:
+        assert cs.STATUS_NAMES[rc] == "CFG_ERR_CUDA", (rc, msg)
+        assert "cudaGetDevice" in msg, msg
