@@ -2,21 +2,27 @@
 
 A "step" is one call of the fused step kernel: rel-MAE + schedule update +
 guidance + DDIM/Euler update over the whole latent of one batch.  The
-default workload is SDXL 1024px, batch 8 (latent 8x4x128x128, bf16 storage,
-50-step DDIM, w = 5).  Inputs are synthetic and resident in HBM; the timed
-steps rotate over enough buffer sets that every step's inputs come from HBM
-(not the 126 MB L2), and are replayed from CUDA graphs.
+default workload is the largest: the video latent 2x16x13x90x160 (bf16
+storage, 50-step DDIM, eta = 0, w = 6).  Inputs are synthetic and resident in
+HBM; the steps rotate over enough buffer sets that every step's inputs come
+from HBM (not the 126 MB L2).  K = --steps steps form one CUDA graph with
+programmatic dependent launch; --replays (>= 10) such graphs run back to back,
+each timed by CUDA events, and the line reports the median per-step time.
 
 Prints ONE JSON line (rank 0):
   value / unit       latent elements per second per step, whole job
   roofline           algorithmic HBM bytes / measured step time vs the measured copy peak
   e2e                the same metric through the public Python API with pinned host
                      buffers, host->device and device->host copies inside the timed region
-  cpu_baseline       the CPU oracle timed on a bounded sample (rank 0, N = 1)
-  sweep              the same device measurement on every other workload, and the default
-                     workload as a batched call with a schedule per sample (rank 0, N = 1)
-  sampler_run        whole 50-step runs through the public API with a synthetic denoiser:
-                     eager host loop, captured CUDA graph, two branch streams (rank 0, N = 1)
+  cpu_baseline       the CPU oracle timed on a bounded sample, the host's core count and CPU
+                     model, and one whole oracle run on a slice of the latent (rank 0, N = 1)
+  sweep              the same device measurement on every other workload, the eta = 1
+                     workload at eta = 0 (its noise-free floor), and the default workload as a
+                     batched call with a schedule per sample (rank 0, N = 1)
+  sampler_run        whole runs of every workload through the public API with a synthetic
+                     denoiser, as a captured CUDA graph, with the denoiser alone timed the same
+                     way; the default workload also as the eager host loop and with two branch
+                     streams (rank 0, N = 1)
 
 ``--impl reference`` times the CPU oracle instead (the slow reference program)
 and prints the same kind of line with ``"impl": "reference"``.
@@ -27,6 +33,7 @@ independent replicas (weak scaling): barrier, time, max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -45,7 +52,7 @@ sys.path.insert(0, str(ROOT))
 
 import workloads as W  # noqa: E402
 
-DEFAULT_WORKLOAD = "sdxl_1024_b8_bf16"
+DEFAULT_WORKLOAD = "video_b2_bf16"
 FALLBACK_HBM_GBS = 6400.0
 PROFILE_DIR = ROOT / "profiles"
 KERNEL_SRC = ROOT / "cfg_guided_sampler_step_b300" / "csrc" / "cfgstep.cu"
@@ -231,13 +238,33 @@ def make_sets(wl, n_sets, device, torch):
     return sets
 
 
-def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clocks=None,
-                sets=None, batch=1):
-    """Time exactly `steps` fused steps (plus `warmup` untimed) over rotating HBM-resident sets.
+def replay_plan(K: int, n_sets: int, n_steps: int, max_graphs: int = 400):
+    """Distinct K-step graphs needed so that back-to-back replays continue one sequence.
 
-    `sets` overrides the number of buffer sets (default: >= 4x the L2 in whole sampler runs);
-    fewer sets keep a profiler capture small and are not used for timing.  `batch` > 1 times
-    the batched step (a rel-MAE and schedule per sample).
+    Step p of the sequence uses buffer set p % n_sets and sampler step p % n_steps, so a
+    set is reused only after every other set has passed; graph g covers steps
+    [gK, (g+1)K) modulo the period lcm(K, n_sets, n_steps).  Returns (graphs, period).
+    """
+    period = math.lcm(K, n_sets, n_steps)
+    D = period // K
+    if D > max_graphs:
+        raise SystemExit(f"--steps {K} needs {D} distinct graphs over {n_sets} buffer sets; "
+                         f"choose a divisor or multiple of {n_sets}")
+    return D, period
+
+
+def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clocks=None,
+                sets=None, batch=1, replays: int = 15, eta=None):
+    """Median per-step time of `replays` timed replays of K = `steps` fused steps.
+
+    The steps rotate over HBM-resident buffer sets (default: >= 4x the L2 in whole sampler
+    runs), so every step reads its inputs from HBM.  Each replay is one CUDA graph of K steps
+    with programmatic dependent launch; the replays run back to back on one stream and each
+    is timed by its own pair of CUDA events, after >= `warmup` untimed steps that also
+    replay (and so upload) every graph once.  Consecutive replays continue one sequence of
+    sampler steps, so each step's deferred reduction is completed by the next launch as in a
+    sampler run.  `sets` overrides the number of buffer sets (fewer only to keep a profiler
+    capture small); `batch` > 1 times the batched step; `eta` overrides the workload's eta.
     """
     import torch
     import cfg_guided_sampler_step_b300 as cs
@@ -249,7 +276,9 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
     n_sets = wl.n_steps * math.ceil(n_sets / wl.n_steps)
     if sets:
         n_sets = int(sets)
-    sets = make_sets(wl, n_sets, device, torch)
+    K = max(1, int(steps))
+    D, period = replay_plan(K, n_sets, wl.n_steps)
+    bufs = make_sets(wl, n_sets, device, torch)
     code = cs.CFG_F32 if wl.dtype == "f32" else cs.CFG_BF16
     ws = cs.new_workspace(wl.n, code, device, batch=batch)
     st = cs.new_sched_state(device, batch=batch)
@@ -257,72 +286,59 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
     sp = cs.SchedParams(n_steps=wl.n_steps, L=wl.L, g_slope=wl.g_slope, k=wl.k, tau_cap=wl.tau_cap,
                         defer=True)
     plan = step_plan(wl, cs)
-    # graph step j uses buffer set j % n_sets (read x_in, pred_c, pred_u; write x_out) and
-    # sampler step j % N.  A graph is one rotation over the sets = whole sampler runs, so a
-    # set is reused only after every other set has passed (>= 4x L2 of traffic in between)
-    # and every replay ends on a run's last step (which finishes its reduction in-launch).
-    # A graph of a partial run ends with a workspace flush, so no step's work is left over.
-    G = n_sets
+    wl_eta = wl if eta is None else dataclasses.replace(wl, eta=eta)
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
 
-    def capture(count):
-        g = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream(device)
-        s.wait_stream(torch.cuda.current_stream(device))
-        with torch.cuda.stream(s):
-            for j in range(min(count, 8)):          # eager warm-up of the launch path
-                enqueue_step(cs, wl, sets[j % n_sets], plan[j % wl.n_steps], ws, st, sp,
-                             batch=batch)
-            cs.workspace_flush(ws, batch=batch)
-        torch.cuda.current_stream(device).wait_stream(s)
-        torch.cuda.synchronize(device)
-        with torch.cuda.graph(g, stream=s):
-            for j in range(count):
-                enqueue_step(cs, wl, sets[j % n_sets], plan[j % wl.n_steps], ws, st, sp,
-                             batch=batch)
-            if count % wl.n_steps:
-                cs.workspace_flush(ws, batch=batch)
-        torch.cuda.synchronize(device)
-        return g
+    def enqueue(p):
+        enqueue_step(cs, wl_eta, bufs[p % n_sets], plan[p % wl.n_steps], ws, st, sp, batch=batch,
+                     stream=s)
 
-    if steps < G:
-        G = steps
-    g_full = capture(G) if G > 0 else None
-    rem = steps % G if G else 0
-    g_rem = capture(rem) if rem else None
-    full_reps = steps // G if G else 0
-    w_full, w_rem = divmod(max(warmup, 0), G) if G else (0, 0)
-    g_wrem = capture(w_rem) if w_rem else None
-    stream = torch.cuda.current_stream(device)
-    for _ in range(w_full):
-        g_full.replay()
-    if g_wrem is not None:
-        g_wrem.replay()
+    with torch.cuda.stream(s):                      # eager warm-up of the launch path
+        for p in range(wl.n_steps):
+            enqueue(p)
+    torch.cuda.synchronize(device)
+    graphs = []
+    for g in range(D):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            for j in range(K):
+                enqueue(g * K + j)
+        graphs.append(gr)
+    torch.cuda.synchronize(device)
+    # warm-up: whole cycles over every graph (each replayed, hence uploaded, once or more)
+    cycles = max(1, math.ceil(max(warmup, 3) / (D * K)))
+    with torch.cuda.stream(s):
+        for _ in range(cycles):
+            for gr in graphs:
+                gr.replay()
     torch.cuda.synchronize(device)
     barrier(world)
     torch.cuda.synchronize(device)
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(replays)]
     if clocks:
         clocks.mark_begin()
-    start.record(stream)
-    for _ in range(full_reps):
-        g_full.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    end.record(stream)
-    end.synchronize()
+    with torch.cuda.stream(s):
+        for r in range(replays):
+            ev[r][0].record(s)
+            graphs[r % D].replay()
+            ev[r][1].record(s)
+    ev[-1][1].synchronize()
     torch.cuda.synchronize(device)
     if clocks:
         clocks.mark_end()
     barrier(world)
-    ms = start.elapsed_time(end)
+    with torch.cuda.stream(s):
+        cs.workspace_flush(ws, batch=batch)
+    torch.cuda.synchronize(device)
+    per_step_ms = sorted(a.elapsed_time(b) / K for a, b in ev)
     state = cs.read_sched_state(st)
-    # launches in the timed region: every step, plus a flush ending each graph of a partial run
-    def graph_launches(count):
-        return count + (1 if count % wl.n_steps else 0) if count else 0
-    launches = full_reps * graph_launches(G) + graph_launches(rem)
-    return {"ms": ms, "n_sets": n_sets, "set_bytes": set_bytes, "l2_bytes": l2,
-            "graph_steps": G, "launches": launches, "state_flags": state["flags"]}
+    return {"ms": statistics.median(per_step_ms) * K, "step_ms_median": statistics.median(per_step_ms),
+            "step_ms_min": per_step_ms[0], "step_ms_max": per_step_ms[-1],
+            "replays": replays, "graph_steps": K, "distinct_graphs": D,
+            "warmup_steps": cycles * D * K, "n_sets": n_sets, "set_bytes": set_bytes,
+            "l2_bytes": l2, "launches": replays * K, "state_flags": state["flags"]}
 
 
 def time_e2e(wl: W.Workload, steps: int, device, depth: int = 3):
@@ -403,13 +419,16 @@ def time_e2e(wl: W.Workload, steps: int, device, depth: int = 3):
             "host_buffers": "page-locked (cfg_host_alloc), copies by cfg_copy_async"}
 
 
-def time_sampler_runs(wl: W.Workload, device, runs: int = 20):
+def time_sampler_runs(wl: W.Workload, device, runs: int = 10, forms: bool = False):
     """Whole sampler runs of the workload through the public API, per denoising step.
 
-    Each step runs a synthetic Gaussian denoiser (fp32 torch ops, the model stand-in) for
-    both branches and the fused step: (1) ``sampler_run``'s host loop, (2) the same run
-    recorded into one CUDA graph and replayed, (3) ``sampler_run_branches`` with the two
-    branches on two streams joined by events.  Reported as microseconds per step.
+    Each step runs a synthetic denoiser (the workload's Gaussian posterior mean, or the flow
+    point mass; fp32 torch ops, the model stand-in) for both branches, then the fused step.
+    The run is recorded into one CUDA graph (``sampler_run`` under stream capture) and
+    replayed; the same denoiser calls without the steps are recorded and replayed too, so
+    the step's share is the difference.  With ``forms``, the eager host loop and
+    ``sampler_run_branches`` (two branch streams joined by events) are timed as well.
+    Microseconds per step, host wall clock around whole runs with the device synchronised.
     """
     import torch
     import cfg_guided_sampler_step_b300 as cs
@@ -442,20 +461,30 @@ def time_sampler_runs(wl: W.Workload, device, runs: int = 20):
               n_steps=wl.n_steps, w=wl.w, pred_c=pc, pred_u=pu, sched=sp, state=st, workspace=ws,
               eta=wl.eta, seed=wl.seed)
     if wl.mode == "ddim":
-        kw["abar_table"] = cs.abar_linear(wl.T, wl.beta_start, wl.beta_end)
-        kw["timesteps"] = cs.ddim_timesteps(wl.n_steps, wl.T)
+        abar = cs.abar_linear(wl.T, wl.beta_start, wl.beta_end)
+        ts = cs.ddim_timesteps(wl.n_steps, wl.T)
+        kw["abar_table"], kw["timesteps"] = abar, ts
+        ts_args = [(s_, int(ts[s_]), float(abar[ts[s_]])) for s_ in range(wl.n_steps)]
+    else:
+        ts_args = [(s_, s_, 1.0 - s_ / wl.n_steps) for s_ in range(wl.n_steps)]
     s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
     sc, su = torch.cuda.Stream(device), torch.cuda.Stream(device)
 
-    def eager():
+    def full():
         x.copy_(x_T)
         cs.sampler_run(x, denoise=both, **kw)
+
+    def denoiser_only():
+        x.copy_(x_T)
+        for a in ts_args:
+            both(*a)
 
     def branches():
         x.copy_(x_T)
         cs.sampler_run_branches(x, denoise_branch=branch, stream_c=sc, stream_u=su, **kw)
 
-    def timed(fn):
+    def wall(fn):
         with torch.cuda.stream(s):
             fn()
             torch.cuda.synchronize(device)
@@ -465,19 +494,20 @@ def time_sampler_runs(wl: W.Workload, device, runs: int = 20):
             torch.cuda.synchronize(device)
         return (time.perf_counter() - t0) / runs / wl.n_steps * 1e6
 
-    res = {"eager_us_per_step": timed(eager), "branch_streams_us_per_step": timed(branches)}
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        eager()
-    g.replay()
-    torch.cuda.synchronize(device)
-    t0 = time.perf_counter()
-    for _ in range(runs):
-        g.replay()
-    torch.cuda.synchronize(device)
-    res["graph_us_per_step"] = (time.perf_counter() - t0) / runs / wl.n_steps * 1e6
-    res["denoiser"] = "synthetic Gaussian posterior-mean denoiser, fp32 torch ops, both branches"
-    res["timer"] = "host wall clock around whole runs, device synchronised"
+    def graph(fn):
+        with torch.cuda.stream(s):
+            fn()                                    # warm-up outside capture
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fn()
+        return wall(g.replay)
+
+    res = {"graph_us_per_step": graph(full), "denoiser_graph_us_per_step": graph(denoiser_only)}
+    res["step_us_per_step"] = res["graph_us_per_step"] - res["denoiser_graph_us_per_step"]
+    if forms:
+        res["eager_us_per_step"] = wall(full)
+        res["branch_streams_us_per_step"] = wall(branches)
     return res
 
 
@@ -582,22 +612,31 @@ def time_randn(n: int, launches: int, warmup: int, device):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400_000)
-    ap.add_argument("--warmup", type=int, default=4_000)
+    ap.add_argument("--steps", type=int, default=100,
+                    help="steps per timed replay (one CUDA graph); the line reports the median "
+                         "per-step time over --replays replays")
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--replays", type=int, default=15)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.WORKLOAD_ORDER)
     ap.add_argument("--impl", default="cfgstep", choices=["cfgstep", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=300)
-    ap.add_argument("--sweep-steps", type=int, default=60_000)
+    ap.add_argument("--sweep-steps", type=int, default=100)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--sets", type=int, default=None,
                     help="buffer sets to rotate over (default: >= 4x L2); fewer only for profiling")
+    ap.add_argument("--eta", type=float, default=None,
+                    help="override the workload's DDIM eta (e.g. 0 for the noise-free floor)")
     ap.add_argument("--randn", type=int, default=None, metavar="N",
                     help="time only the eta-noise stream (cfg_randn, N normals per launch) and exit")
     args = ap.parse_args(argv)
+    if args.replays < 10:
+        ap.error("--replays must be >= 10 (the line reports a median over replays)")
     world, rank, local = dist_env()
     wl = W.WORKLOADS[args.workload]
+    if args.eta is not None:
+        wl = dataclasses.replace(wl, eta=args.eta)
     warmup = max(args.warmup, 3)
     metric = "latent elements/s per CFG sampler step"
     unit = "latent elements/s"
@@ -615,7 +654,7 @@ def main(argv=None):
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": workload_config(wl),
                 "cpu_baseline": {"value": r["value"], "unit": unit, "cores": oracle_threads(),
-                                 "kind": "oracle", "sample": sample},
+                                 "kind": "oracle", "sample": sample, "host": host_info()},
                 "e2e": {"value": r["value"], "unit": unit, "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
@@ -642,27 +681,33 @@ def main(argv=None):
     clocks = ClockSampler(uuid) if rank == 0 else None
     if clocks:
         clocks.start()
-    dev = time_device(wl, args.steps, warmup, device, world, clocks, sets=args.sets)
+    dev = time_device(wl, args.steps, warmup, device, world, clocks, sets=args.sets,
+                      replays=args.replays)
     clk = clocks.stop() if clocks else None
-    ms = max_over_ranks(dev["ms"], world, device)
-    total_elems = sum_over_ranks(float(wl.n * args.steps), world, device)
-    value = total_elems / (ms * 1e-3)
-    per_launch_s = dev["ms"] * 1e-3 / max(args.steps, 1)
+    # the job's per-step time is its slowest rank's; every rank processes one latent per step
+    step_s = max_over_ranks(dev["step_ms_median"], world, device) * 1e-3
+    total_elems = sum_over_ranks(float(wl.n), world, device)
+    value = total_elems / step_s
     peak, peak_kind = hbm_peak()
-    achieved = wl.bytes_per_step / per_launch_s / 1e9
+    achieved = wl.bytes_per_step / (dev["step_ms_median"] * 1e-3) / 1e9
     e2e = time_e2e(wl, args.e2e_steps, device)
     e2e_v = sum_over_ranks(e2e["value"], world, device)
     if rank != 0:
         return 0
     line = {
         "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
-        "warmup": warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "warmup": dev["warmup_steps"], "ms_per_step": step_s * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": dict(workload_config(wl), parallelism=f"replicas{world}",
                        l2=f"rotating {dev['n_sets']} buffer sets of {dev['set_bytes']} B "
                           f"({dev['n_sets'] * dev['set_bytes'] / 2**20:.0f} MiB; the L2 holds "
-                          f"{dev['l2_bytes'] / 2**20:.0f} MiB)",
-                       launch=f"CUDA graphs of {dev['graph_steps']} steps, programmatic dependent launch"),
+                          f"{dev['l2_bytes'] / 2**20:.0f} MiB), inputs larger than L2",
+                       launch=f"CUDA graphs of {dev['graph_steps']} steps, programmatic dependent "
+                              f"launch",
+                       timing=f"median over {dev['replays']} back-to-back replays of a "
+                              f"{dev['graph_steps']}-step graph, each timed by CUDA events; "
+                              f"per-step min {dev['step_ms_min'] * 1e3:.3f} us, max "
+                              f"{dev['step_ms_max'] * 1e3:.3f} us"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(wl.name),
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
@@ -681,36 +726,72 @@ def main(argv=None):
         "clocks": clk,
     }
     if world == 1 and not args.no_sweep:
-        line["sampler_run"] = time_sampler_runs(wl, device)
+        line["sampler_run"] = {name: time_sampler_runs(W.WORKLOADS[name], device,
+                                                       forms=(name == wl.name))
+                               for name in W.WORKLOAD_ORDER}
+        line["sampler_run"]["denoiser"] = ("synthetic posterior-mean / flow point-mass denoiser, "
+                                           "fp32 torch ops, both branches")
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     if world == 1 and not args.no_sweep:
-        sweep = {}
-        for name in W.WORKLOAD_ORDER:
-            if name == wl.name:
-                continue
-            w2 = W.WORKLOADS[name]
-            d2 = time_device(w2, args.sweep_steps, 2000, device, 1)
-            s = d2["ms"] * 1e-3 / args.sweep_steps
-            sweep[name] = {"value": w2.n / s, "us_per_step": s * 1e6,
-                           "achieved_gbs": w2.bytes_per_step / s / 1e9,
-                           "frac": w2.bytes_per_step / s / 1e9 / peak,
-                           "traffic": profiled_traffic(name)}
-        # the default workload again with a rel-MAE and tau1/tau2 schedule per sample
-        if wl.shape[0] > 1:
-            d2 = time_device(wl, args.sweep_steps, 2000, device, 1, batch=wl.shape[0])
-            s = d2["ms"] * 1e-3 / args.sweep_steps
-            sweep[f"{wl.name}/per_sample"] = {
-                "value": wl.n / s, "us_per_step": s * 1e6, "batch": wl.shape[0],
-                "achieved_gbs": wl.bytes_per_step / s / 1e9,
-                "frac": wl.bytes_per_step / s / 1e9 / peak}
-        line["sweep"] = sweep
+        line["sweep"] = sweep(wl, args.sweep_steps, args.replays, device, peak)
     print(json.dumps(line), flush=True)
     return 0
 
 
+def sweep(wl: W.Workload, steps: int, replays: int, device, peak: float):
+    """The same device measurement on every other workload, the 3840px workload without noise
+    (eta = 0, its floor), and the default workload as a batched call with a rel-MAE and
+    schedule per sample."""
+    out = {}
+
+    def row(w2, **kw):
+        d2 = time_device(w2, steps, 100, device, 1, replays=replays, **kw)
+        s = d2["step_ms_median"] * 1e-3
+        return {"value": w2.n / s, "us_per_step": s * 1e6,
+                "us_per_step_min": d2["step_ms_min"] * 1e3,
+                "achieved_gbs": w2.bytes_per_step / s / 1e9,
+                "frac": w2.bytes_per_step / s / 1e9 / peak}
+
+    for name in W.WORKLOAD_ORDER:
+        w2 = W.WORKLOADS[name]
+        if name != wl.name:
+            out[name] = dict(row(w2), traffic=profiled_traffic(name))
+        if w2.eta > 0:
+            out[f"{name}/eta0"] = row(w2, eta=0.0)
+    if wl.shape[0] > 1:
+        out[f"{wl.name}/per_sample"] = dict(row(wl, batch=wl.shape[0]), batch=wl.shape[0])
+    return out
+
+
+def slice_shape(shape, n_target: int):
+    """The leading slice of `shape` (fewer samples, channels, frames ...) with at most
+    n_target elements, keeping at least the last axis."""
+    shape = list(shape)
+    for i in range(len(shape) - 1):
+        if int(np.prod(shape)) <= n_target:
+            break
+        rest = int(np.prod(shape[i + 1:]))
+        shape[i] = max(1, min(shape[i], n_target // rest))
+    return tuple(shape)
+
+
+def host_info():
+    model = None
+    try:
+        for line in Path("/proc/cpuinfo").read_text().splitlines():
+            if line.startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "cpu_model": model}
+
+
 def cpu_baseline(wl: W.Workload, seconds: float):
-    """The oracle's step on the full latent, repeated for about `seconds` on one host core."""
+    """The oracle's step on the full latent, repeated for about `seconds` on one host core,
+    and one whole oracle run (denoiser and steps) on a slice of the latent."""
+    from oracle import cfg_oracle as O
     fn = oracle_step_fn(wl, wl.n)
     fn(0)
     t0 = time.perf_counter()
@@ -721,9 +802,27 @@ def cpu_baseline(wl: W.Workload, seconds: float):
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
+    # a whole run on a leading slice of the latent sized for about `seconds`, from the rate
+    # of a probe run on a small slice
+    def run(shape):
+        sl = wl.scaled(shape)
+        inp = W.draw_inputs(sl)
+        pert = (lambda s_, b: W.draw_perturbation(sl, s_, b)) if sl.perturb_std else None
+        t0 = time.perf_counter()
+        O.run_sampler(sl, inp, perturb=pert)
+        return sl, time.perf_counter() - t0
+
+    probe, t_probe = run(slice_shape(wl.shape, 1 << 16))
+    n_target = int(seconds * probe.n / max(t_probe, 1e-6))
+    sl, run_s = run(slice_shape(wl.shape, max(probe.n, n_target)))
+    shape = sl.shape
     return {"value": wl.n * reps / dt, "unit": "latent elements/s", "cores": oracle_threads(),
             "kind": "oracle",
-            "sample": f"{reps} oracle steps (fp64 NumPy) on the full {wl.n}-element latent, {dt:.1f} s"}
+            "sample": f"{reps} oracle steps (fp64 NumPy) on the full {wl.n}-element latent, {dt:.1f} s",
+            "host": host_info(),
+            "full_run": {"shape": list(shape), "n": sl.n, "steps": sl.n_steps,
+                         "seconds": run_s, "latent_elements_per_s": sl.n * sl.n_steps / run_s,
+                         "what": "oracle run_sampler: synthetic denoiser and step, every step"}}
 
 
 def workload_config(wl: W.Workload):
