@@ -21,14 +21,14 @@ from typing import Callable, Dict, Optional
 import numpy as np
 
 __all__ = [
-    "CFG_F32", "CFG_BF16", "CFG_MODE_DDIM", "CFG_MODE_FLOW", "TAU_NONE", "SCHED_MAX_STEPS",
+    "CFG_F32", "CFG_BF16", "CFG_BF16_EXACT", "CFG_MODE_DDIM", "CFG_MODE_FLOW", "TAU_NONE", "SCHED_MAX_STEPS",
     "CfgError", "SchedParams", "lib", "lib_path", "workspace_bytes", "new_workspace",
     "new_sched_state", "read_sched_state", "workspace_flush", "SCHED_DEFER", "relmae_reduce", "ddim_step", "flow_step",
     "sched_observe", "randn", "abar_linear", "ddim_timesteps", "abar_cosine", "timesteps",
     "sampler_run", "sampler_run_branches", "version", "pinned_empty", "copy_async",
 ]
 
-CFG_F32, CFG_BF16 = 0, 1
+CFG_F32, CFG_BF16, CFG_BF16_EXACT = 0, 1, 2
 SCHED_DEFER = 1
 SCHED_FLAG_OUT_OF_ORDER, SCHED_FLAG_DEFER_CLASH = 1, 2
 CFG_MODE_DDIM, CFG_MODE_FLOW = 0, 1
@@ -146,12 +146,14 @@ def _torch():
     return torch
 
 
-def _dtype_code(t) -> int:
+def _dtype_code(t, exact_rounding: bool = False) -> int:
+    """Storage code of a tensor; ``exact_rounding`` selects CFG_BF16_EXACT for bf16 (the step
+    rounds the exact value correctly; fp32 steps are compensated either way)."""
     torch = _torch()
     if t.dtype == torch.float32:
         return CFG_F32
     if t.dtype == torch.bfloat16:
-        return CFG_BF16
+        return CFG_BF16_EXACT if exact_rounding else CFG_BF16
     raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
 
 
@@ -269,39 +271,44 @@ def _same(x_out, x_in, pc, pu) -> None:
 
 def ddim_step(x_out, x_in, pred_c, pred_u, *, w: float, abar_t: float, abar_prev: float,
               workspace, eta: float = 0.0, seed: int = 0, step: int = 0, M_out=None, state=None,
-              sched=None, stream=None, batch: int = 1) -> None:
-    """One fused CFG + DDIM step (see cfg_ddim_step; batch > 1: cfg_ddim_step_batched)."""
+              sched=None, stream=None, batch: int = 1, exact_rounding: bool = False) -> None:
+    """One fused CFG + DDIM step (see cfg_ddim_step; batch > 1: cfg_ddim_step_batched).
+    ``exact_rounding``: bf16 results correctly rounded (CFG_BF16_EXACT)."""
     _same(x_out, x_in, pred_c, pred_u)
     ws, wsb = _ws(workspace)
     _check(lib.cfg_ddim_step_batched(
         _dev_ptr(x_out, "x_out"), _dev_ptr(x_in, "x_in"), _dev_ptr(pred_c, "pred_c"),
-        _dev_ptr(pred_u, "pred_u"), _per_sample(x_out, batch), batch, _dtype_code(x_out), w,
-        abar_t, abar_prev, eta, seed, step, _dev_ptr(M_out, "M_out"), _dev_ptr(state, "state"),
+        _dev_ptr(pred_u, "pred_u"), _per_sample(x_out, batch), batch,
+        _dtype_code(x_out, exact_rounding), w, abar_t, abar_prev, eta, seed, step, _dev_ptr(M_out, "M_out"), _dev_ptr(state, "state"),
         _sp(sched), ws, wsb, _stream(stream)))
 
 
 def ddim_step_static_ws(x_out, x_in, pred_c, pred_u, *, w: float, abar_t: float,
                         abar_prev: float, eta: float = 0.0, seed: int = 0, step: int = 0,
-                        M_out=None, state=None, sched=None, stream=None) -> None:
+                        M_out=None, state=None, sched=None, stream=None,
+                        exact_rounding: bool = False) -> None:
     """ddim_step on the library's static device scratch (no workspace argument), for callers
     that cannot allocate device memory; calls on one device share that scratch."""
     _same(x_out, x_in, pred_c, pred_u)
     _check(lib.cfg_ddim_step_static_ws(
         _dev_ptr(x_out, "x_out"), _dev_ptr(x_in, "x_in"), _dev_ptr(pred_c, "pred_c"),
-        _dev_ptr(pred_u, "pred_u"), x_out.numel(), _dtype_code(x_out), w, abar_t, abar_prev, eta,
+        _dev_ptr(pred_u, "pred_u"), x_out.numel(), _dtype_code(x_out, exact_rounding), w, abar_t,
+        abar_prev, eta,
         seed, step, _dev_ptr(M_out, "M_out"), _dev_ptr(state, "state"), _sp(sched),
         _stream(stream)))
 
 
 def flow_step(x_out, x_in, v_c, v_u, *, w: float, t_cur: float, t_next: float, workspace,
               step: int = 0, M_out=None, state=None, sched=None, stream=None,
-              batch: int = 1) -> None:
-    """One fused CFG + Euler flow step (see cfg_flow_step; batch > 1: cfg_flow_step_batched)."""
+              batch: int = 1, exact_rounding: bool = False) -> None:
+    """One fused CFG + Euler flow step (see cfg_flow_step; batch > 1: cfg_flow_step_batched).
+    ``exact_rounding``: bf16 results correctly rounded (CFG_BF16_EXACT)."""
     _same(x_out, x_in, v_c, v_u)
     ws, wsb = _ws(workspace)
     _check(lib.cfg_flow_step_batched(
         _dev_ptr(x_out, "x_out"), _dev_ptr(x_in, "x_in"), _dev_ptr(v_c, "v_c"),
-        _dev_ptr(v_u, "v_u"), _per_sample(x_out, batch), batch, _dtype_code(x_out), w, t_cur,
+        _dev_ptr(v_u, "v_u"), _per_sample(x_out, batch), batch,
+        _dtype_code(x_out, exact_rounding), w, t_cur,
         t_next, step, _dev_ptr(M_out, "M_out"), _dev_ptr(state, "state"), _sp(sched), ws, wsb,
         _stream(stream)))
 
@@ -400,7 +407,8 @@ def timesteps(n_steps: int, T: int = 1000, spacing: str = "linspace") -> np.ndar
 def sampler_run(x, *, mode: int, n_steps: int, w: float, denoise: Callable, pred_c, pred_u,
                 sched: SchedParams, state, workspace, abar_table: Optional[np.ndarray] = None,
                 timesteps: Optional[np.ndarray] = None, t_grid: Optional[np.ndarray] = None,
-                eta: float = 0.0, seed: int = 0, start_step: int = 0, stream=None) -> None:
+                eta: float = 0.0, seed: int = 0, start_step: int = 0, stream=None,
+                exact_rounding: bool = False) -> None:
     """Run a whole CFG sampler in the library's host loop (see cfg_sampler_run).
 
     ``denoise(step, timestep, t)`` must enqueue the two predictions for the
@@ -433,7 +441,7 @@ def sampler_run(x, *, mode: int, n_steps: int, w: float, denoise: Callable, pred
         tg = t_grid.ctypes.data_as(POINTER(c_double))
     ws, wsb = _ws(workspace)
     status = lib.cfg_sampler_run(
-        _dev_ptr(x, "x"), x.numel(), _dtype_code(x), mode, ab,
+        _dev_ptr(x, "x"), x.numel(), _dtype_code(x, exact_rounding), mode, ab,
         0 if abar_table is None else int(abar_table.shape[0]), ts, tg, n_steps, w, eta, seed, cb,
         None, _dev_ptr(pred_c, "pred_c"), _dev_ptr(pred_u, "pred_u"), _sp(sched),
         _dev_ptr(state, "state"), start_step, ws, wsb, _stream(stream))
@@ -447,7 +455,7 @@ def sampler_run_branches(x, *, mode: int, n_steps: int, w: float, denoise_branch
                          workspace, abar_table: Optional[np.ndarray] = None,
                          timesteps: Optional[np.ndarray] = None,
                          t_grid: Optional[np.ndarray] = None, eta: float = 0.0, seed: int = 0,
-                         start_step: int = 0, stream=None) -> None:
+                         start_step: int = 0, stream=None, exact_rounding: bool = False) -> None:
     """A whole CFG sampler run with the two branches on two streams (see
     cfg_sampler_run_branches).
 
@@ -482,7 +490,7 @@ def sampler_run_branches(x, *, mode: int, n_steps: int, w: float, denoise_branch
         tg = t_grid.ctypes.data_as(POINTER(c_double))
     ws, wsb = _ws(workspace)
     status = lib.cfg_sampler_run_branches(
-        _dev_ptr(x, "x"), x.numel(), _dtype_code(x), mode, ab,
+        _dev_ptr(x, "x"), x.numel(), _dtype_code(x, exact_rounding), mode, ab,
         0 if abar_table is None else int(abar_table.shape[0]), ts, tg, n_steps, w, eta, seed, cb,
         None, _dev_ptr(pred_c, "pred_c"), _dev_ptr(pred_u, "pred_u"), _stream(stream_c),
         _stream(stream_u), _sp(sched), _dev_ptr(state, "state"), start_step, ws, wsb,

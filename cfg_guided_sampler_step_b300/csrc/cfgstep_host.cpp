@@ -24,8 +24,9 @@ using cfgstep::fail;
 namespace {
 
 int check_dtype(int32_t dtype) {
-  if (dtype != CFG_F32 && dtype != CFG_BF16)
-    return fail(CFG_ERR_UNSUPPORTED_DTYPE, "unsupported dtype %d (CFG_F32=0, CFG_BF16=1)", dtype);
+  if (dtype != CFG_F32 && dtype != CFG_BF16 && dtype != CFG_BF16_EXACT)
+    return fail(CFG_ERR_UNSUPPORTED_DTYPE,
+                "unsupported dtype %d (CFG_F32=0, CFG_BF16=1, CFG_BF16_EXACT=2)", dtype);
   return CFG_OK;
 }
 

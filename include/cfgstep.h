@@ -60,8 +60,13 @@ extern "C" {
 #define CFG_API
 #endif
 
-/* Storage types. */
-enum cfg_dtype { CFG_F32 = 0, CFG_BF16 = 1 };
+/* Storage types.  CFG_BF16 and CFG_BF16_EXACT store the same bf16 values in
+ * memory and differ only in how a step rounds its result (see
+ * cfg_ddim_step): CFG_BF16 rounds the fp32 evaluation of the step once
+ * (within one bf16 ulp of the exact step); CFG_BF16_EXACT rounds the exact
+ * step correctly (as an fp64 evaluation rounded once to bf16), at some cost
+ * in time.  Reductions treat the two alike. */
+enum cfg_dtype { CFG_F32 = 0, CFG_BF16 = 1, CFG_BF16_EXACT = 2 };
 
 /* Sampler kinds for cfg_sampler_run. */
 enum cfg_mode { CFG_MODE_DDIM = 0, CFG_MODE_FLOW = 1 };
@@ -70,7 +75,7 @@ enum cfg_mode { CFG_MODE_DDIM = 0, CFG_MODE_FLOW = 1 };
 enum cfg_status {
   CFG_OK = 0,
   CFG_ERR_INVALID_ARG = -1,       /* a pointer, size or parameter is out of range */
-  CFG_ERR_UNSUPPORTED_DTYPE = -2, /* dtype is not CFG_F32 / CFG_BF16 */
+  CFG_ERR_UNSUPPORTED_DTYPE = -2, /* dtype is not one of cfg_dtype */
   CFG_ERR_WORKSPACE = -3,         /* workspace missing, too small or misaligned */
   CFG_ERR_CUDA = -4,              /* the CUDA runtime returned an error */
   CFG_ERR_CALLBACK = -5           /* the denoiser callback returned non-zero */
@@ -221,7 +226,11 @@ CFG_API int cfg_relmae_reduce(const void* pred_c, const void* pred_u, int64_t n,
  * abar_prev = 1 makes this the last step (x_out = x0).  z ~ N(0,1) is drawn
  * in registers from Philox4x32-10 with key = seed and counter
  * (i/4 low word, i/4 high word, step, 0) and Box-Muller on 23-bit uniforms
- * (see cfg_randn), so it costs no memory traffic and is reproducible.
+ * (see cfg_randn), so it costs no memory traffic and is reproducible.  The
+ * integer stream is cfg_randn's exactly; the Gaussian transform is evaluated
+ * to the accuracy the storage needs: within a few fp32 ulps for fp32
+ * storage (as cfg_randn), within about 5e-6 absolute for bf16 storage (both
+ * bf16 types; the result keeps 8 significant bits).
  * Fused with the rel-MAE of (pred_c, pred_u) and, when st is given, the
  * schedule update for step `step`: one pass reading x, pred_c, pred_u and
  * writing x_out (4n elements of traffic).
@@ -233,10 +242,20 @@ CFG_API int cfg_relmae_reduce(const void* pred_c, const void* pred_u, int64_t n,
  *   eta             >= 0, finite;
  *   seed, step      Philox key and counter word (step >= 0);
  *   M_out           device double, nullable;  st, sp: see cfg_relmae_reduce.
- * Arithmetic: fp32 for bf16 storage; for fp32 storage, compensated
- * (double-fp32) arithmetic so the stored result is the fp32 rounding of the
- * exact step in all but rare near-tie cases.  The coefficients are formed
- * in fp64 on the host.
+ * Rounding, by storage type (the exact step: for the given inputs, the
+ * coefficients formed in fp64 on the host, and the drawn z):
+ *   CFG_BF16        fp32 arithmetic rounded once to bf16: within one bf16
+ *                   ulp of the exact step, equal to its correct rounding
+ *                   except where the fp32 evaluation error crosses a
+ *                   rounding midpoint;
+ *   CFG_BF16_EXACT  the same fp32 evaluation with a per-element error bound;
+ *                   the few elements (a few per thousand) whose result lies
+ *                   within that bound of a bf16 rounding midpoint are
+ *                   recomputed in double-fp32 (about 2^-44 of the step's
+ *                   terms), so every element is the correct rounding of the
+ *                   exact step unless that lies this close to a midpoint;
+ *   CFG_F32         double-fp32 arithmetic rounded once: the fp32 value
+ *                   nearest the exact step in all but rare near-tie cases.
  */
 CFG_API int cfg_ddim_step(void* x_out, const void* x_in, const void* pred_c, const void* pred_u,
                           int64_t n, int32_t dtype, float w, double abar_t, double abar_prev,
@@ -425,7 +444,8 @@ CFG_API int cfg_sampler_run_branches(void* x, int64_t n, int32_t dtype, int32_t 
  * u = (2 (r >> 9) + 1) / 2^24.  The DDIM step uses stream_id 0.  The integer
  * stream is exact; the transform is evaluated in fp32 (exact integer range
  * reduction, short series for ln and sin/cos) to within a few fp32 ulps of
- * the exact values.
+ * the exact values (bf16-storage steps use a cheaper transform of the same
+ * integers; see cfg_ddim_step).
  *   out: device float, n elements (n >= 0).
  */
 CFG_API int cfg_randn(float* out, int64_t n, uint64_t seed, uint32_t step, uint32_t stream_id,

@@ -40,3 +40,23 @@ def cuda():
         pytest.skip("no CUDA device")
     import torch
     return torch.device("cuda:0")
+
+
+_PARITY_ROWS = {}
+
+
+@pytest.fixture(scope="session")
+def parity_report():
+    """Collects per-case parity figures (errors, margins) measured by the GPU tests; when the
+    environment names a file in CFG_PARITY_REPORT, they are written there as JSON at the end
+    of the session (the figures quoted in the design notes come from such a file)."""
+    return _PARITY_ROWS
+
+
+def pytest_sessionfinish(session, exitstatus):
+    import json
+    import os
+    path = os.environ.get("CFG_PARITY_REPORT")
+    if path and _PARITY_ROWS:
+        Path(path).parent.mkdir(parents=True, exist_ok=True)
+        Path(path).write_text(json.dumps(_PARITY_ROWS, indent=1, sort_keys=True, default=float))

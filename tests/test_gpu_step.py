@@ -9,8 +9,11 @@ same stored values.  Tolerances:
   arithmetic for fp32 storage); with eta > 0 the noise itself is an fp32
   Box-Muller value (relative error ~4e-7), so only the 1e-5 bound applies;
 * bf16 storage: max |g - o| / max(|o|, 1) <= 2e-2, and every element within
-  1 bf16 ulp (fp32 arithmetic, one final rounding) unless cancellation left
-  a result below the fp32 arithmetic's absolute error;
+  1 bf16 ulp unless cancellation left a result below the fp32 arithmetic's
+  absolute error (2^-17); correctly rounded (CFG_BF16_EXACT) and without
+  noise, every element equal to the oracle's bf16 value (the oracle's fp64
+  step rounded once), except where the exact value lies within 2^-40 of a
+  rounding midpoint, certified by exact rational arithmetic;
 * rel-MAE: relative error <= 1e-6 (fp32 L1 partial sums with Kahan
   compensation, fp64 combine).
 """
@@ -25,7 +28,8 @@ import torch
 import cfg_guided_sampler_step_b300 as cs
 import workloads as W
 from oracle import cfg_oracle as O
-from gpu_harness import TORCH_DTYPE, rel_err, to_device_stored, to_host_f64, ulp_distance_bf16, ulp_distance_f32
+from gpu_harness import (TORCH_DTYPE, certify_bf16_mismatches, ddim_exact, flow_exact, rel_err,
+                         to_device_stored, to_host_f64, ulp_distance_bf16, ulp_distance_f32)
 
 pytestmark = pytest.mark.gpu
 GOLDEN = Path(__file__).parent / "golden"
@@ -54,11 +58,13 @@ def _inputs(n, dtype, seed, cuda, offset=0):
     return out
 
 
-def _compare(got, ref, dtype, strict_ulp):
+def _compare(got, ref, dtype, strict_ulp, exact_bf16=None):
     """Stated tolerance, plus (strict_ulp) every element within 1 ulp of the oracle's stored
     value or, where the result is tiny after cancellation, within the arithmetic's absolute
-    error bound (fp32 arithmetic: 3 * 2^-24 * |terms| <= 2^-17 for |terms| <= 20;
-    compensated fp32: <= 1e-9)."""
+    error bound (fp32 noise in the bf16 step: 2^-17; compensated fp32: <= 1e-9), plus
+    (exact_bf16: the step's exact value, see gpu_harness.ddim_exact / flow_exact) every bf16
+    element equal to the oracle's except where the exact value lies within 2^-40 of the
+    midpoint between the two (both are correct roundings there)."""
     if got.size == 0:
         return
     diff = np.abs(got - ref)
@@ -72,12 +78,20 @@ def _compare(got, ref, dtype, strict_ulp):
         if strict_ulp:
             ok = (ulp_distance_bf16(got, ref) <= 1) | (diff <= 2.0**-17)
             assert ok.all(), np.flatnonzero(~ok)[:10]
+        if exact_bf16 is not None:
+            bad = certify_bf16_mismatches(got, ref, exact_bf16)
+            assert bad.size == 0, (bad[:10], got[bad[:10]], ref[bad[:10]])
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+# storage under test: fp32, bf16 with the default rounding, bf16 correctly rounded
+STORAGES = [("f32", False), ("bf16", False), ("bf16", True)]
+STORAGE_IDS = ["f32", "bf16", "bf16_exact"]
+
+
+@pytest.mark.parametrize("dtype,exact", STORAGES, ids=STORAGE_IDS)
 @pytest.mark.parametrize("n", SIZES)
 @pytest.mark.parametrize("eta", [0.0, 1.0])
-def test_ddim_step_matches_oracle(cuda, dtype, n, eta):
+def test_ddim_step_matches_oracle(cuda, dtype, exact, n, eta):
     d = _inputs(n, dtype, seed=100 + n % 97, cuda=cuda)
     abar = O.abar_linear()
     ab, abp = float(abar[500]), float(abar[480])
@@ -86,10 +100,12 @@ def test_ddim_step_matches_oracle(cuda, dtype, n, eta):
     M = torch.zeros(1, dtype=torch.float64, device=cuda)
     ws = cs.new_workspace(n, _code(dtype), cuda)
     cs.ddim_step(x_out, d["x"], d["c"], d["u"], w=w, abar_t=ab, abar_prev=abp, eta=eta, seed=seed,
-                 step=step, M_out=M, workspace=ws)
+                 step=step, M_out=M, workspace=ws, exact_rounding=exact)
     torch.cuda.synchronize()
     ref, refM = O.ddim_step(d["x64"], d["c64"], d["u64"], dtype, w, ab, abp, eta, seed, step)
-    _compare(to_host_f64(x_out), ref, dtype, strict_ulp=(eta == 0.0))
+    _compare(to_host_f64(x_out), ref, dtype, strict_ulp=(eta == 0.0 or dtype == "bf16"),
+             exact_bf16=ddim_exact(d["x64"], d["c64"], d["u64"], w, ab, abp)
+             if (exact and eta == 0.0) else None)
     gotM = float(M.item())
     if n == 0:
         assert gotM == 0.0 and refM == 0.0
@@ -97,24 +113,26 @@ def test_ddim_step_matches_oracle(cuda, dtype, n, eta):
         assert abs(gotM - refM) <= 1e-6 * refM
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype,exact", STORAGES, ids=STORAGE_IDS)
 @pytest.mark.parametrize("n", [1, 9, 4097, 1 << 20])
-def test_ddim_last_step_and_in_place(cuda, dtype, n):
+def test_ddim_last_step_and_in_place(cuda, dtype, exact, n):
     """abar_prev = 1 returns the x0 prediction; x_out may alias x_in."""
     d = _inputs(n, dtype, seed=7, cuda=cuda)
     ab = float(O.abar_linear()[0])
     ws = cs.new_workspace(n, _code(dtype), cuda)
     x = d["x"].clone()
     cs.ddim_step(x, x, d["c"], d["u"], w=6.0, abar_t=ab, abar_prev=1.0, eta=1.0, seed=3, step=49,
-                 workspace=ws)
+                 workspace=ws, exact_rounding=exact)
     torch.cuda.synchronize()
     ref, _ = O.ddim_step(d["x64"], d["c64"], d["u64"], dtype, 6.0, ab, 1.0, 1.0, 3, 49, last=True)
-    _compare(to_host_f64(x), ref, dtype, strict_ulp=True)
+    _compare(to_host_f64(x), ref, dtype, strict_ulp=True,
+             exact_bf16=ddim_exact(d["x64"], d["c64"], d["u64"], 6.0, ab, 1.0) if exact else None)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype,exact", STORAGES, ids=STORAGE_IDS)
 @pytest.mark.parametrize("offset", [1, 3])
-def test_misaligned_pointers_take_the_scalar_path(cuda, dtype, offset):
+@pytest.mark.parametrize("eta", [0.0, 1.0])
+def test_misaligned_pointers_take_the_scalar_path(cuda, dtype, exact, offset, eta):
     n = 50_000 + 3
     d = _inputs(n, dtype, seed=11, cuda=cuda, offset=offset)
     assert d["x"].data_ptr() % 16 != 0
@@ -123,27 +141,30 @@ def test_misaligned_pointers_take_the_scalar_path(cuda, dtype, offset):
     x_out = torch.empty(n + 1, dtype=TORCH_DTYPE[dtype], device=cuda)[1:]
     M = torch.zeros(1, dtype=torch.float64, device=cuda)
     ws = cs.new_workspace(n, _code(dtype), cuda)
-    cs.ddim_step(x_out, d["x"], d["c"], d["u"], w=5.0, abar_t=ab, abar_prev=abp, eta=1.0, seed=5,
-                 step=2, M_out=M, workspace=ws)
+    cs.ddim_step(x_out, d["x"], d["c"], d["u"], w=5.0, abar_t=ab, abar_prev=abp, eta=eta, seed=5,
+                 step=2, M_out=M, workspace=ws, exact_rounding=exact)
     torch.cuda.synchronize()
-    ref, refM = O.ddim_step(d["x64"], d["c64"], d["u64"], dtype, 5.0, ab, abp, 1.0, 5, 2)
-    _compare(to_host_f64(x_out), ref, dtype, strict_ulp=False)
+    ref, refM = O.ddim_step(d["x64"], d["c64"], d["u64"], dtype, 5.0, ab, abp, eta, 5, 2)
+    _compare(to_host_f64(x_out), ref, dtype, strict_ulp=(eta == 0.0 or dtype == "bf16"),
+             exact_bf16=ddim_exact(d["x64"], d["c64"], d["u64"], 5.0, ab, abp)
+             if (exact and eta == 0.0) else None)
     assert abs(M.item() - refM) <= 1e-6 * refM
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype,exact", STORAGES, ids=STORAGE_IDS)
 @pytest.mark.parametrize("n", [0, 1, 9, 4097, 1 << 20, 3 * (1 << 20) + 5])
-def test_flow_step_matches_oracle(cuda, dtype, n):
+def test_flow_step_matches_oracle(cuda, dtype, exact, n):
     d = _inputs(n, dtype, seed=200 + n % 13, cuda=cuda)
     t_cur, t_next = 1.0 - 3 / 28, 1.0 - 4 / 28
     x_out = torch.empty_like(d["x"])
     M = torch.zeros(1, dtype=torch.float64, device=cuda)
     ws = cs.new_workspace(n, _code(dtype), cuda)
     cs.flow_step(x_out, d["x"], d["c"], d["u"], w=3.5, t_cur=t_cur, t_next=t_next, M_out=M,
-                 workspace=ws)
+                 workspace=ws, exact_rounding=exact)
     torch.cuda.synchronize()
     ref, refM = O.flow_step(d["x64"], d["c64"], d["u64"], dtype, 3.5, t_cur, t_next)
-    _compare(to_host_f64(x_out), ref, dtype, strict_ulp=True)
+    _compare(to_host_f64(x_out), ref, dtype, strict_ulp=True,
+             exact_bf16=flow_exact(d["x64"], d["c64"], d["u64"], 3.5, t_cur, t_next) if exact else None)
     if n:
         assert abs(M.item() - refM) <= 1e-6 * refM
 
