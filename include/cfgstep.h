@@ -251,9 +251,14 @@ CFG_API int cfg_relmae_reduce(const void* pred_c, const void* pred_u, int64_t n,
  *   CFG_BF16_EXACT  the same fp32 evaluation with a per-element error bound;
  *                   the few elements (a few per thousand) whose result lies
  *                   within that bound of a bf16 rounding midpoint are
- *                   recomputed in double-fp32 (about 2^-44 of the step's
- *                   terms), so every element is the correct rounding of the
- *                   exact step unless that lies this close to a midpoint;
+ *                   recomputed: without noise as the pages write the step,
+ *                   in fp64 one correctly rounded operation at a time
+ *                   (e = u + w (c - u); x0 = (x - sqrt(1 - abar_t) e) /
+ *                   sqrt(abar_t); sqrt(abar_prev) x0 + sqrt(1 - abar_prev) e,
+ *                   or x0 on the last step), with noise in double-fp32
+ *                   (about 2^-44 of the step's terms); so every element is
+ *                   what an fp64 evaluation of the step rounded once to bf16
+ *                   gives (without noise: exactly that);
  *   CFG_F32         double-fp32 arithmetic rounded once: the fp32 value
  *                   nearest the exact step in all but rare near-tie cases.
  */

@@ -14,23 +14,19 @@ stored x_T, means and perturbations.  Checked:
   crosses a rounding midpoint now and then gives a 1-ulp split from the
   oracle's trajectory, which the bf16-stored predictions carry forward,
   amplified by w: the per-element bound holds for the SDXL and fp32 runs and
-  is recorded, not asserted, for the others.  Correctly rounded, DDIM runs
-  without noise follow the oracle's trajectory bit for bit (asserted); with
+  is recorded, not asserted, for the others (for the flow workload the splits
+  are frequent: with dt = t_next - t_cur close to -1/28 and w = 7/2, about 2%
+  of the Euler steps' exact values lie within 2^-40 of a bf16 midpoint, since
+  v/28 is dyadic whenever 7 divides v, and the bf16-stored velocities amplify
+  a split by 1/t).  Correctly rounded, runs without noise follow the oracle's
+  trajectory bit for bit, the flow workload included (asserted: the library
+  decides its near-midpoint elements with the oracle's fp64 evaluation); with
   eta > 0 the fp32 noise (within about 5e-6 of the oracle's fp64 transform)
-  splits an element now and then, and the per-element bound holds.  The flow
-  workload is the exception to the per-element bound in both modes: with
-  dt = t_next - t_cur close to -1/28 and w = 7/2, about 2% of the Euler steps'
-  exact values lie within 2^-40 of a bf16 midpoint (v/28 is dyadic whenever
-  7 divides v), where the oracle's fp64 evaluation and the library's
-  double-fp32 one each pick a correct neighbour by their own rounding; the
-  bf16-stored velocities then amplify the split (a 1-ulp change of x moves
-  (x - m)/t by 1/t).  Teacher-forced, every flow step is checked element by
-  element, with every difference certified as such a midpoint case by exact
-  rational arithmetic;
+  splits an element now and then, and the per-element bound holds;
 * the rel-MAE trace: fp32 abs <= 1e-5 and rel <= 1e-6; bf16 rel <= 1e-9
   correctly rounded without noise (the same trajectory), otherwise <= 3e-5
   for DDIM (the trajectories differ by rare 1-ulp splits) and <= 1e-3 for
-  flow (the midpoint splits);
+  flow with the default rounding (the midpoint splits);
 * tau1', tau_cap, tau1, tau2, decided_at and the phases: exactly equal to
   the oracle's, and the oracle's rule applied to the device's own M trace
   reproduces the device's G values bit for bit.
@@ -104,9 +100,9 @@ def _check(wl, inputs, gpu, ref, report=None, key=None, exact=False):
         assert fig["M_abs_max"] <= 1e-5, fig
         assert fig["M_rel_max"] <= 1e-6, fig
     else:
-        if wl.mode != "flow" and (exact or base in DEFAULT_ROUNDING_ELEMENTWISE):
+        if exact or (wl.mode != "flow" and base in DEFAULT_ROUNDING_ELEMENTWISE):
             assert fig["x_rel_elem_max"] <= 2e-2, fig
-        if exact and wl.mode != "flow" and wl.eta == 0.0:
+        if exact and wl.eta == 0.0:
             assert fig["ulp_max"] == 0 and fig["M_rel_max"] <= 1e-9, fig   # the same trajectory
         assert fig["x_rel_norm2"] <= 2e-2, fig
         assert fig["x_rel_maxnorm"] <= 2e-2, fig
@@ -185,8 +181,8 @@ def _teacher_forced(wl, inputs, cuda, exact=False):
     """Every step of the oracle's run, replayed through the library on the oracle's own
     stored x_s and predictions: each output element within 1 ulp of the oracle's x_{s+1}
     (or, after cancellation to a tiny value, within 2^-17 for bf16 / 1e-9 for fp32), and,
-    correctly rounded (``exact``) without noise, equal to it except at certified midpoints;
-    each M_s within 1e-6 relative."""
+    correctly rounded (``exact``) without noise, equal to it; each M_s within 1e-6
+    relative."""
     pert = _perturb(wl)
     ref = O.run_sampler(wl, inputs, perturb=pert, keep_trajectory=True)
     reps = wl.n // inputs["mean_c"].size
@@ -232,8 +228,8 @@ def _teacher_forced(wl, inputs, cuda, exact=False):
                 # no noise: correctly rounded, equal to the oracle except at certified midpoints
                 ex = (flow_exact(x, c, u, wl.w, float(tg[s]), float(tg[s + 1])) if wl.mode == "flow"
                       else ddim_exact(x, c, u, wl.w, ab, abp))
-                bad = certify_bf16_mismatches(g, o, ex, limit=200000)
-                assert bad.size == 0, (s, bad[:5])
+                bad = np.flatnonzero(g != o)
+                assert bad.size == 0, (s, bad[:5], certify_bf16_mismatches(g, o, ex, limit=200000)[:5])
         else:
             assert float(diff.max()) <= 1e-5
             ok = (ulp_distance_f32(g, o) <= 1) | (diff <= 1e-9)
