@@ -55,7 +55,8 @@ import workloads as W  # noqa: E402
 DEFAULT_WORKLOAD = "video_b2_bf16"
 FALLBACK_HBM_GBS = 6400.0
 PROFILE_DIR = ROOT / "profiles"
-KERNEL_SRC = ROOT / "cfg_guided_sampler_step_b300" / "csrc" / "cfgstep.cu"
+KERNEL_SRC = (ROOT / "cfg_guided_sampler_step_b300" / "csrc" / "cfgstep.cu",
+              ROOT / "cfg_guided_sampler_step_b300" / "csrc" / "cfg_noise.cuh")
 
 
 # ---------------------------------------------------------------------------
@@ -115,7 +116,11 @@ def hbm_peak():
 
 
 def kernel_source_hash() -> str:
-    return hashlib.sha256(KERNEL_SRC.read_bytes()).hexdigest()[:16]
+    """sha256[:16] of the step kernel's sources (the kernel file, then the noise header)."""
+    h = hashlib.sha256()
+    for f in KERNEL_SRC:
+        h.update(f.read_bytes())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload: str):

@@ -18,6 +18,7 @@ REPO_DIR = PKG_DIR.parent
 SRC = PKG_DIR / "csrc" / "cfgstep.cu"
 SOURCES = [SRC, PKG_DIR / "csrc" / "cfgstep_host.cpp"]
 INTERNAL = PKG_DIR / "csrc" / "cfgstep_internal.h"
+NOISE = PKG_DIR / "csrc" / "cfg_noise.cuh"
 HEADER = REPO_DIR / "include" / "cfgstep.h"
 LIB = PKG_DIR / "libcfgstep.so"
 
@@ -47,7 +48,7 @@ def needs_build() -> bool:
     if not LIB.exists():
         return True
     t = LIB.stat().st_mtime
-    return any(p.stat().st_mtime > t for p in (*SOURCES, INTERNAL, HEADER, Path(__file__)))
+    return any(p.stat().st_mtime > t for p in (*SOURCES, INTERNAL, NOISE, HEADER, Path(__file__)))
 
 
 def build(force: bool = False, verbose: bool = False) -> Path:

@@ -21,7 +21,7 @@ stored x_T, means and perturbations.  Checked:
   a split by 1/t).  Correctly rounded, runs without noise follow the oracle's
   trajectory bit for bit, the flow workload included (asserted: the library
   decides its near-midpoint elements with the oracle's fp64 evaluation); with
-  eta > 0 the fp32 noise (within about 5e-6 of the oracle's fp64 transform)
+  eta > 0 the fp32 noise (within 3.2e-6 of the oracle's fp64 transform)
   splits an element now and then, and the per-element bound holds;
 * the rel-MAE trace: fp32 abs <= 1e-5 and rel <= 1e-6; bf16 rel <= 1e-9
   correctly rounded without noise (the same trajectory), otherwise <= 3e-5
