@@ -5,9 +5,11 @@ guidance + DDIM/Euler update over the whole latent of one batch.  The
 default workload is the largest: the video latent 2x16x13x90x160 (bf16
 storage, 50-step DDIM, eta = 0, w = 6).  Inputs are synthetic and resident in
 HBM; the steps rotate over enough buffer sets that every step's inputs come
-from HBM (not the 126 MB L2).  K = --steps steps form one CUDA graph with
-programmatic dependent launch; --replays (>= 10) such graphs run back to back,
-each timed by CUDA events, and the line reports the median per-step time.
+from HBM (not the 126 MB L2).  K steps form one CUDA graph with programmatic
+dependent launch (K = --steps rounded up to a multiple of itself of at least
+100: a graph boundary costs about one step); --replays (>= 10) such graphs run
+back to back, each timed by CUDA events, and the line reports the median
+per-step time.
 
 Prints ONE JSON line (rank 0):
   value / unit       latent elements per second per step, whole job
@@ -243,6 +245,9 @@ def make_sets(wl, n_sets, device, torch):
     return sets
 
 
+MIN_GRAPH_STEPS = 100
+
+
 def replay_plan(K: int, n_sets: int, n_steps: int, max_graphs: int = 400):
     """Distinct K-step graphs needed so that back-to-back replays continue one sequence.
 
@@ -259,8 +264,9 @@ def replay_plan(K: int, n_sets: int, n_steps: int, max_graphs: int = 400):
 
 
 def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clocks=None,
-                sets=None, batch=1, replays: int = 15, eta=None):
-    """Median per-step time of `replays` timed replays of K = `steps` fused steps.
+                sets=None, batch=1, replays: int = 15, eta=None, min_seconds: float = 0.0):
+    """Median per-step time of `replays` timed replays of K fused steps (K = `steps` rounded
+    up to a multiple of itself of at least MIN_GRAPH_STEPS).
 
     The steps rotate over HBM-resident buffer sets (default: >= 4x the L2 in whole sampler
     runs), so every step reads its inputs from HBM.  Each replay is one CUDA graph of K steps
@@ -269,7 +275,9 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
     replay (and so upload) every graph once.  Consecutive replays continue one sequence of
     sampler steps, so each step's deferred reduction is completed by the next launch as in a
     sampler run.  `sets` overrides the number of buffer sets (fewer only to keep a profiler
-    capture small); `batch` > 1 times the batched step; `eta` overrides the workload's eta.
+    capture small); `batch` > 1 times the batched step; `eta` overrides the workload's eta;
+    `min_seconds` raises the replay count until the timed region lasts that long (so the clock
+    sampler sees it several times; the line still reports the median replay).
     """
     import torch
     import cfg_guided_sampler_step_b300 as cs
@@ -281,7 +289,12 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
     n_sets = wl.n_steps * math.ceil(n_sets / wl.n_steps)
     if sets:
         n_sets = int(sets)
+    # A graph boundary costs about one step (programmatic dependent launch does not overlap
+    # steps across graph launches: 8.81 / 8.54 / 8.46 / 8.43 us per video step in graphs of
+    # 20 / 50 / 100 / 200 steps, measured), so each timed replay is a graph of at least
+    # MIN_GRAPH_STEPS steps: `steps` rounded up to a multiple of itself.
     K = max(1, int(steps))
+    K *= math.ceil(MIN_GRAPH_STEPS / K)
     D, period = replay_plan(K, n_sets, wl.n_steps)
     bufs = make_sets(wl, n_sets, device, torch)
     code = cs.CFG_F32 if wl.dtype == "f32" else cs.CFG_BF16
@@ -318,6 +331,21 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
             for gr in graphs:
                 gr.replay()
     torch.cuda.synchronize(device)
+    cycles_extra = 0
+    if min_seconds > 0:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            a.record(s)
+            for gr in graphs:
+                gr.replay()
+            b.record(s)
+        b.synchronize()
+        per_replay_s = a.elapsed_time(b) * 1e-3 / len(graphs)
+        cycles_extra = D * K
+        replays = max(replays, min(20000, math.ceil(min_seconds / max(per_replay_s, 1e-9))))
+    # every rank times the same number of replays
+    replays = int(max_over_ranks(float(replays), world, device))
+    torch.cuda.synchronize(device)
     barrier(world)
     torch.cuda.synchronize(device)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -342,7 +370,7 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
     return {"ms": statistics.median(per_step_ms) * K, "step_ms_median": statistics.median(per_step_ms),
             "step_ms_min": per_step_ms[0], "step_ms_max": per_step_ms[-1],
             "replays": replays, "graph_steps": K, "distinct_graphs": D,
-            "warmup_steps": cycles * D * K, "n_sets": n_sets, "set_bytes": set_bytes,
+            "warmup_steps": cycles * D * K + cycles_extra, "n_sets": n_sets, "set_bytes": set_bytes,
             "l2_bytes": l2, "launches": replays * K, "state_flags": state["flags"]}
 
 
@@ -618,10 +646,13 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100,
-                    help="steps per timed replay (one CUDA graph); the line reports the median "
+                    help="steps per timed replay (one CUDA graph), rounded up to a multiple of "
+                         f"itself of at least {MIN_GRAPH_STEPS}; the line reports the median "
                          "per-step time over --replays replays")
     ap.add_argument("--warmup", type=int, default=100)
     ap.add_argument("--replays", type=int, default=15)
+    ap.add_argument("--min-seconds", type=float, default=0.5,
+                    help="more replays until the timed region lasts this long (clock samples)")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.WORKLOAD_ORDER)
     ap.add_argument("--impl", default="cfgstep", choices=["cfgstep", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=300)
@@ -687,7 +718,7 @@ def main(argv=None):
     if clocks:
         clocks.start()
     dev = time_device(wl, args.steps, warmup, device, world, clocks, sets=args.sets,
-                      replays=args.replays)
+                      replays=args.replays, min_seconds=args.min_seconds)
     clk = clocks.stop() if clocks else None
     # the job's per-step time is its slowest rank's; every rank processes one latent per step
     step_s = max_over_ranks(dev["step_ms_median"], world, device) * 1e-3
@@ -710,7 +741,9 @@ def main(argv=None):
                        launch=f"CUDA graphs of {dev['graph_steps']} steps, programmatic dependent "
                               f"launch",
                        timing=f"median over {dev['replays']} back-to-back replays of a "
-                              f"{dev['graph_steps']}-step graph, each timed by CUDA events; "
+                              f"{dev['graph_steps']}-step graph (--steps {args.steps} rounded up "
+                              f"to a multiple of at least {MIN_GRAPH_STEPS}: a graph boundary "
+                              f"costs about one step), each timed by CUDA events; "
                               f"per-step min {dev['step_ms_min'] * 1e3:.3f} us, max "
                               f"{dev['step_ms_max'] * 1e3:.3f} us"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
