@@ -117,11 +117,20 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_only(text: str) -> str:
+    """C++/CUDA source with comments, trailing blanks and blank lines removed (the kernel
+    sources hold no comment markers inside string literals)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash() -> str:
-    """sha256[:16] of the step kernel's sources (the kernel file, then the noise header)."""
+    """sha256[:16] of the step kernel's code (the kernel file, then the noise header; comments
+    and blank lines excluded, so a change of wording does not void a profile)."""
     h = hashlib.sha256()
     for f in KERNEL_SRC:
-        h.update(f.read_bytes())
+        h.update(code_only(f.read_text()).encode())
     return h.hexdigest()[:16]
 
 
@@ -131,7 +140,7 @@ def profiled_traffic(workload: str):
     if not f.exists():
         return None
     text = f.read_text()
-    m_src = re.search(r"kernel source sha256\[:16\]\s*\|\s*`?([0-9a-f]{16})", text)
+    m_src = re.search(r"kernel source sha256\[:16\][^|\n]*\|\s*`?([0-9a-f]{16})", text)
     m_b = re.search(r"dram bytes per launch \(read \+ write\)\s*\|\s*([0-9][0-9,]*)", text)
     if not m_src or not m_b or m_src.group(1) != kernel_source_hash():
         return None
@@ -248,6 +257,13 @@ def make_sets(wl, n_sets, device, torch):
 MIN_GRAPH_STEPS = 100
 
 
+def graph_length(steps: int) -> int:
+    """Steps in one timed graph: `steps` rounded up to a multiple of itself of at least
+    MIN_GRAPH_STEPS (a graph boundary costs about one step)."""
+    k = max(1, int(steps))
+    return k * math.ceil(MIN_GRAPH_STEPS / k)
+
+
 def replay_plan(K: int, n_sets: int, n_steps: int, max_graphs: int = 400):
     """Distinct K-step graphs needed so that back-to-back replays continue one sequence.
 
@@ -293,8 +309,7 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
     # steps across graph launches: 8.81 / 8.54 / 8.46 / 8.43 us per video step in graphs of
     # 20 / 50 / 100 / 200 steps, measured), so each timed replay is a graph of at least
     # MIN_GRAPH_STEPS steps: `steps` rounded up to a multiple of itself.
-    K = max(1, int(steps))
-    K *= math.ceil(MIN_GRAPH_STEPS / K)
+    K = graph_length(steps)
     D, period = replay_plan(K, n_sets, wl.n_steps)
     bufs = make_sets(wl, n_sets, device, torch)
     code = cs.CFG_F32 if wl.dtype == "f32" else cs.CFG_BF16

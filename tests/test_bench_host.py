@@ -74,3 +74,21 @@ def test_peak_and_profile_readers():
     assert peak > 1000 and kind in ("measured", "fallback")
     assert len(bench.kernel_source_hash()) == 16
     assert bench.profiled_traffic("no_such_workload") is None
+
+
+def test_kernel_hash_ignores_comments_but_not_code():
+    sys.path.insert(0, str(ROOT))
+    import bench
+    src = "// header\nint f(int a) {  /* the sum\n of two */\n  return a + 1;  // one\n}\n\n"
+    assert bench.code_only(src) == bench.code_only(src.replace("the sum", "a sum").replace("// one", ""))
+    assert bench.code_only(src) != bench.code_only(src.replace("a + 1", "a + 2"))
+    assert bench.code_only(src) == "int f(int a) {\n  return a + 1;\n}"
+
+
+def test_graph_length_rounds_up_to_whole_multiples():
+    sys.path.insert(0, str(ROOT))
+    import bench
+    assert [bench.graph_length(k) for k in (1, 7, 20, 30, 100, 150, 0)] == [100, 105, 100, 120, 100, 150, 100]
+    for k in range(1, 260):
+        g = bench.graph_length(k)
+        assert g % k == 0 and g >= bench.MIN_GRAPH_STEPS and g - k < bench.MIN_GRAPH_STEPS
