@@ -337,7 +337,7 @@ def pinned_empty(numel: int, dtype) -> "torch.Tensor":
 
     Copies from/to it with :func:`copy_async` run asynchronously in stream order.  (torch's
     ``is_pinned()`` reports only its own pool, so it says False here, and ``Tensor.copy_``
-    treats the memory as pageable; the driver knows it is page-locked.)
+    treats the memory as pageable; the CUDA driver knows it is page-locked.)
     """
     torch = _torch()
     itemsize = torch.empty((), dtype=dtype).element_size()

@@ -512,7 +512,7 @@ CFG_API int cfg_host_free(void* p);
  * memory (cudaMemcpyAsync, direction from the pointers) on `stream`.  With a
  * page-locked host side (cfg_host_alloc) it returns at once and the copy
  * runs in stream order, overlapping other streams' work; with pageable host
- * memory the driver stages it and the call may block.
+ * memory the CUDA driver stages it and the call may block.
  *   dst, src: non-NULL unless bytes == 0 (then a no-op); the ranges must not
  *   overlap.  CFG_ERR_CUDA if the runtime rejects the copy.
  */

@@ -28,7 +28,7 @@ def test_pinned_empty_is_page_locked_and_round_trips(cuda):
     n = 3 * (1 << 20) + 5
     h = cs.pinned_empty(n, torch.bfloat16)
     assert h.device.type == "cpu" and h.dtype == torch.bfloat16 and h.numel() == n
-    # page-locked as far as the driver is concerned (torch's is_pinned only knows its own pool)
+    # page-locked as far as the CUDA driver is concerned (torch's is_pinned only knows its own pool)
     from cuda.bindings import runtime as cudart
     err, attr = cudart.cudaPointerGetAttributes(h.data_ptr())
     assert err == cudart.cudaError_t.cudaSuccess
