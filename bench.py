@@ -228,17 +228,17 @@ def step_plan(wl: W.Workload, cs):
     return [dict(step=s, t_cur=1.0 - s / N, t_next=1.0 - (s + 1) / N) for s in range(N)]
 
 
-def enqueue_step(cs, wl, bufs, plan_s, ws, st, sp, M=None, batch=1, stream=None):
+def enqueue_step(cs, wl, bufs, plan_s, ws, st, sp, M=None, batch=1, stream=None, exact=False):
     x, pc, pu = bufs[:3]
     xo = bufs[3] if len(bufs) > 3 else x
     if wl.mode == "ddim":
         cs.ddim_step(xo, x, pc, pu, w=wl.w, abar_t=plan_s["abar_t"], abar_prev=plan_s["abar_prev"],
                      eta=wl.eta, seed=wl.seed, step=plan_s["step"], M_out=M, state=st, sched=sp,
-                     workspace=ws, batch=batch, stream=stream)
+                     workspace=ws, batch=batch, stream=stream, exact_rounding=exact)
     else:
         cs.flow_step(xo, x, pc, pu, w=wl.w, t_cur=plan_s["t_cur"], t_next=plan_s["t_next"],
                      step=plan_s["step"], M_out=M, state=st, sched=sp, workspace=ws, batch=batch,
-                     stream=stream)
+                     stream=stream, exact_rounding=exact)
 
 
 def make_sets(wl, n_sets, device, torch):
@@ -280,7 +280,8 @@ def replay_plan(K: int, n_sets: int, n_steps: int, max_graphs: int = 400):
 
 
 def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clocks=None,
-                sets=None, batch=1, replays: int = 15, eta=None, min_seconds: float = 0.0):
+                sets=None, batch=1, replays: int = 15, eta=None, min_seconds: float = 0.0,
+                exact: bool = False):
     """Median per-step time of `replays` timed replays of K fused steps (K = `steps` rounded
     up to a multiple of itself of at least MIN_GRAPH_STEPS).
 
@@ -293,7 +294,8 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
     sampler run.  `sets` overrides the number of buffer sets (fewer only to keep a profiler
     capture small); `batch` > 1 times the batched step; `eta` overrides the workload's eta;
     `min_seconds` raises the replay count until the timed region lasts that long (so the clock
-    sampler sees it several times; the line still reports the median replay).
+    sampler sees it several times; the line still reports the median replay); `exact` times the
+    correctly rounded bf16 steps (CFG_BF16_EXACT).
     """
     import torch
     import cfg_guided_sampler_step_b300 as cs
@@ -325,7 +327,7 @@ def time_device(wl: W.Workload, steps: int, warmup: int, device, world: int, clo
 
     def enqueue(p):
         enqueue_step(cs, wl_eta, bufs[p % n_sets], plan[p % wl.n_steps], ws, st, sp, batch=batch,
-                     stream=s)
+                     stream=s, exact=exact)
 
     with torch.cuda.stream(s):                      # eager warm-up of the launch path
         for p in range(wl.n_steps):
@@ -794,8 +796,8 @@ def main(argv=None):
 
 def sweep(wl: W.Workload, steps: int, replays: int, device, peak: float):
     """The same device measurement on every other workload, the 3840px workload without noise
-    (eta = 0, its floor), and the default workload as a batched call with a rel-MAE and
-    schedule per sample."""
+    (eta = 0, its floor), the default workload as a batched call with a rel-MAE and schedule
+    per sample, and every bf16 workload with correctly rounded steps (CFG_BF16_EXACT)."""
     out = {}
 
     def row(w2, **kw):
@@ -814,6 +816,9 @@ def sweep(wl: W.Workload, steps: int, replays: int, device, peak: float):
             out[f"{name}/eta0"] = row(w2, eta=0.0)
     if wl.shape[0] > 1:
         out[f"{wl.name}/per_sample"] = dict(row(wl, batch=wl.shape[0]), batch=wl.shape[0])
+    for name in W.WORKLOAD_ORDER:
+        if W.WORKLOADS[name].dtype == "bf16":
+            out[f"{name}/exact"] = row(W.WORKLOADS[name], exact=True)
     return out
 
 
