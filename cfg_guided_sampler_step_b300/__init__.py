@@ -12,7 +12,6 @@ missing -- there is no fallback path.
 from __future__ import annotations
 
 import ctypes
-import math
 from ctypes import (CFUNCTYPE, POINTER, Structure, c_char_p, c_double, c_float, c_int32, c_int64,
                     c_size_t, c_uint8, c_uint32, c_uint64, c_void_p)
 from pathlib import Path
