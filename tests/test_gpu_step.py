@@ -621,3 +621,29 @@ def test_step_beyond_2_31_elements(cuda):
     assert ok.all(), idx[~ok][:10]
     del x, u, c, out
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("exact", [False, True], ids=["bf16", "bf16_exact"])
+def test_every_element_on_a_rounding_midpoint(cuda, exact):
+    """A flow step whose exact result is a bf16 rounding midpoint at (nearly) every element:
+    x = +-(1 + j 2^-7), v = c = -2^-6 (w = 1, u = 0) and dt = t_next - t_cur = -1/4, so
+    x + dt v = x + 2^-8, half a bf16 ulp from x.  Ties go to even (the pages' fp64 step rounded
+    once, as the oracle does), so even last bits stay and odd ones round to the neighbour.
+    Correctly rounded, every element lies near a midpoint: each block's queue of near elements
+    overflows, and the rest are recomputed by the thread that found them.  Every element must
+    equal the oracle's in both roundings."""
+    n = 3 * (1 << 20) + 5
+    rng = np.random.default_rng(11)
+    j = rng.integers(0, 128, n)
+    x64 = np.where(rng.random(n) < 0.5, -1.0, 1.0) * (1.0 + j * 2.0**-7)
+    c64, u64 = np.full(n, -2.0**-6), np.zeros(n)
+    x, c, u = (torch.from_numpy(v).to(torch.bfloat16).to(cuda) for v in (x64, c64, u64))
+    out = torch.empty_like(x)
+    ws = cs.new_workspace(n, cs.CFG_BF16, cuda)
+    cs.flow_step(out, x, c, u, w=1.0, t_cur=0.5, t_next=0.25, workspace=ws, exact_rounding=exact)
+    torch.cuda.synchronize()
+    ref, _ = O.flow_step(x64, c64, u64, "bf16", 1.0, 0.5, 0.25)
+    got = to_host_f64(out)
+    assert np.mean(np.abs(ref - x64) > 0) > 0.4          # about half the ties round away
+    bad = np.flatnonzero(got != ref)
+    assert bad.size == 0, (bad[:10], got[bad[:10]], ref[bad[:10]], x64[bad[:10]])
