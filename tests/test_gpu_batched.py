@@ -29,10 +29,15 @@ def _pair(n, dtype, seed, cuda):
     return dev, f64
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+# storage under test: fp32, bf16 with the default rounding, bf16 correctly rounded
+STORAGES = [("f32", False), ("bf16", False), ("bf16", True)]
+STORAGE_IDS = ["f32", "bf16", "bf16_exact"]
+
+
+@pytest.mark.parametrize("dtype,exact", STORAGES, ids=STORAGE_IDS)
 @pytest.mark.parametrize("batch,n_ps", [(1, 4096), (3, 4096), (8, 65536), (5, 1003), (2, 3 * 2**18 + 8)])
 @pytest.mark.parametrize("eta", [0.0, 1.0])
-def test_batched_ddim_step(cuda, dtype, batch, n_ps, eta):
+def test_batched_ddim_step(cuda, dtype, exact, batch, n_ps, eta):
     n = batch * n_ps
     d, f = _pair(n, dtype, 600 + batch + n_ps % 97, cuda)
     abar = O.abar_linear()
@@ -41,20 +46,25 @@ def test_batched_ddim_step(cuda, dtype, batch, n_ps, eta):
     M1 = torch.zeros(1, dtype=torch.float64, device=cuda)
     MB = torch.full((batch,), -1.0, dtype=torch.float64, device=cuda)
     cs.ddim_step(ref_out, d["x"], d["c"], d["u"], w=6.0, abar_t=ab, abar_prev=abp, eta=eta, seed=5,
-                 step=7, M_out=M1, workspace=cs.new_workspace(n, _code(dtype), cuda))
+                 step=7, M_out=M1, workspace=cs.new_workspace(n, _code(dtype), cuda),
+                 exact_rounding=exact)
     cs.ddim_step(out, d["x"], d["c"], d["u"], w=6.0, abar_t=ab, abar_prev=abp, eta=eta, seed=5,
                  step=7, M_out=MB, workspace=cs.new_workspace(n, _code(dtype), cuda, batch=batch),
-                 batch=batch)
+                 batch=batch, exact_rounding=exact)
     torch.cuda.synchronize()
     assert torch.equal(out, ref_out)                 # the update is the unbatched step's
+    if exact and eta == 0.0:                         # correctly rounded: the oracle's, element by element
+        want, _ = O.ddim_step(f["x"], f["c"], f["u"], "bf16", 6.0, ab, abp, 0.0, 5, 7)
+        bad = np.flatnonzero(to_host_f64(out) != want)
+        assert bad.size == 0, bad[:10]
     ref = O.rel_mae_per_sample(f["c"], f["u"], batch)
     got = MB.cpu().numpy()
     assert np.all(np.abs(got / ref - 1) <= 1e-6), (got, ref)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype,exact", STORAGES, ids=STORAGE_IDS)
 @pytest.mark.parametrize("batch,n_ps", [(4, 4096), (3, 777)])
-def test_batched_flow_step_and_reduce(cuda, dtype, batch, n_ps):
+def test_batched_flow_step_and_reduce(cuda, dtype, exact, batch, n_ps):
     n = batch * n_ps
     d, f = _pair(n, dtype, 700 + batch, cuda)
     ref_out, out = torch.empty_like(d["x"]), torch.empty_like(d["x"])
@@ -62,12 +72,16 @@ def test_batched_flow_step_and_reduce(cuda, dtype, batch, n_ps):
     MR = torch.full((batch,), -1.0, dtype=torch.float64, device=cuda)
     ws = cs.new_workspace(n, _code(dtype), cuda, batch=batch)
     cs.flow_step(ref_out, d["x"], d["c"], d["u"], w=3.5, t_cur=0.5, t_next=0.45,
-                 workspace=cs.new_workspace(n, _code(dtype), cuda))
+                 workspace=cs.new_workspace(n, _code(dtype), cuda), exact_rounding=exact)
     cs.flow_step(out, d["x"], d["c"], d["u"], w=3.5, t_cur=0.5, t_next=0.45, M_out=MB,
-                 workspace=ws, batch=batch)
+                 workspace=ws, batch=batch, exact_rounding=exact)
     cs.relmae_reduce(d["c"], d["u"], M_out=MR, workspace=ws, batch=batch)
     torch.cuda.synchronize()
     assert torch.equal(out, ref_out)
+    if exact:                                        # correctly rounded: the oracle's, element by element
+        want, _ = O.flow_step(f["x"], f["c"], f["u"], "bf16", 3.5, 0.5, 0.45)
+        bad = np.flatnonzero(to_host_f64(out) != want)
+        assert bad.size == 0, bad[:10]
     ref = O.rel_mae_per_sample(f["c"], f["u"], batch)
     for M in (MB, MR):
         assert np.all(np.abs(M.cpu().numpy() / ref - 1) <= 1e-6)
