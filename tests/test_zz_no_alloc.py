@@ -8,8 +8,9 @@ the one before left in it):
 * against the CPU oracle's step (``O.ddim_step``) on the same stored inputs, at the
   single-step tolerances: fp32 max |error| <= 1e-5 and, for eta = 0, every element within
   1 ulp (or 1e-9 after cancellation); bf16 max |g - o| / max(|o|, 1) <= 2e-2 and every
-  element within 1 bf16 ulp (or 2^-17 after cancellation); rel-MAE within 1e-6 relative;
-  the schedule state against the oracle's rule on the oracle's rel-MAE trace;
+  element within 1 bf16 ulp (or 2^-17 after cancellation), and with CFG_BF16_EXACT every
+  noise-free result equal to the oracle's; rel-MAE within 1e-6 relative; the schedule state
+  against the oracle's rule on the oracle's rel-MAE trace;
 * against cfg_ddim_step on a caller-owned workspace, bit for bit (x, M and the state).
 
 Called through the C ABI directly and through the Python wrapper, and back to back on one
@@ -36,8 +37,11 @@ CALLS = [(1_000_003, 1.0), (65_536 + 7, 0.0), (4097, 1.0)]
 W_SCALE, SEED = 6.0, 11
 
 
-def _check_oracle(got, ref, dtype, eta):
+def _check_oracle(got, ref, dtype, eta, exact=False, last=False):
     diff = np.abs(got - ref)
+    if exact and (eta == 0.0 or last):
+        bad = np.flatnonzero(got != ref)
+        assert bad.size == 0, bad[:10]
     if dtype == "f32":
         assert float(diff.max()) <= 1e-5, float(diff.max())
         if eta == 0.0:
@@ -55,10 +59,11 @@ def _abar_pair(call):
     return float(abar[600 - 20 * call]), (1.0 if last else float(abar[580 - 20 * call]))
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_static_scratch_step_matches_oracle_and_workspace_step(cuda, dtype):
+@pytest.mark.parametrize("storage", ["bf16", "f32", "bf16_exact"])
+def test_static_scratch_step_matches_oracle_and_workspace_step(cuda, storage):
     """Independent inputs per call, through the C ABI, each call synchronised."""
-    code = cs.CFG_F32 if dtype == "f32" else cs.CFG_BF16
+    dtype, exact = ("f32", False) if storage == "f32" else ("bf16", storage == "bf16_exact")
+    code = cs.CFG_F32 if dtype == "f32" else (cs.CFG_BF16_EXACT if exact else cs.CFG_BF16)
     sp = cs.SchedParams(n_steps=len(CALLS), L=1, g_slope=1.0, k=2)
     st_ref, st_new = cs.new_sched_state(cuda), cs.new_sched_state(cuda)
     stream = torch.cuda.current_stream().cuda_stream
@@ -72,7 +77,7 @@ def test_static_scratch_step_matches_oracle_and_workspace_step(cuda, dtype):
         new_M = torch.full((1,), -1.0, dtype=torch.float64, device=cuda)
         cs.ddim_step(ref_out, x, c, u, w=W_SCALE, abar_t=ab, abar_prev=abp, eta=eta, seed=SEED,
                      step=call, M_out=ref_M, state=st_ref, sched=sp,
-                     workspace=cs.new_workspace(n, code, cuda))
+                     workspace=cs.new_workspace(n, code, cuda), exact_rounding=exact)
         rc = cs.lib.cfg_ddim_step_static_ws(
             new_out.data_ptr(), x.data_ptr(), c.data_ptr(), u.data_ptr(), n, code, W_SCALE, ab,
             abp, eta, SEED, call, new_M.data_ptr(), st_new.data_ptr(), ctypes.byref(sp.c), stream)
@@ -84,7 +89,7 @@ def test_static_scratch_step_matches_oracle_and_workspace_step(cuda, dtype):
         f64 = {k: W.stored_to_f64(d[k], dtype) for k in ("x", "c", "u")}
         ref, refM = O.ddim_step(f64["x"], f64["c"], f64["u"], dtype, W_SCALE, ab, abp, eta, SEED,
                                 call, last=(abp == 1.0))
-        _check_oracle(got, ref, dtype, eta)
+        _check_oracle(got, ref, dtype, eta, exact=exact, last=(abp == 1.0))
         assert abs(new_M.item() / refM - 1) <= 1e-6, call
         oracle_M.append(refM)
     a, b = cs.read_sched_state(st_ref), cs.read_sched_state(st_new)
